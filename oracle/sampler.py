@@ -1,0 +1,105 @@
+"""The per-position vocab sampler of one denoising step, fp64.
+
+Test infrastructure only (see the package docstring).
+
+What is computed ([AIT] §섹션별 상세, the sampling-loop paragraph; [AB]
+§블록 자동 회귀 노이즈 제거 및 자체 수정; [AIT] glossary, self-conditioning):
+
+1. z = logits / temperature; p = softmax(z) per position (row);
+2. entropy H = -sum p ln p (0 ln 0 = 0), argmax (lowest index on ties),
+   confidence = max p;
+3. entropy-bound decision: a position whose entropy is below the bound is
+   committed to its argmax token; the others are renoised to a uniformly
+   random token (uniform-state renoise);
+4. self-conditioning soft embedding: soft_emb = P E, the probability-weighted
+   embedding of every position.
+
+Readings (listed in the design notes): the commit test is strict, H < bound,
+per position (``commit_mode=0``); ``commit_mode=1`` instead commits the longest
+run of qualifying positions from the left of each canvas (the page's "fix the
+low-entropy prefix" wording).  Frozen positions keep their token, count as
+committed and still contribute to the soft embedding.  The random token is
+splitmix.renoise_token(seed, step, row), row = flattened position b*C + i.
+With ``probs_storage='bf16'`` the probabilities are rounded to bf16 before the
+product with E (they are stored in bf16 for that product).
+"""
+from __future__ import annotations
+
+from typing import Iterable, Optional
+
+import numpy as np
+
+from .numerics import bf16_round
+from .splitmix import renoise_token
+
+
+def row_statistics(logits_row: np.ndarray, temperature: float = 1.0):
+    """Softmax, entropy, argmax and confidence of one row, exactly in fp64."""
+    z = np.asarray(logits_row, np.float64) / temperature
+    a = int(np.argmax(z))            # numpy returns the first (lowest) index of the max
+    m = z[a]
+    e = np.exp(z - m)
+    Z = np.sum(e)
+    p = e / Z
+    with np.errstate(divide="ignore", invalid="ignore"):
+        plogp = np.where(p > 0, p * np.log(np.where(p > 0, p, 1.0)), 0.0)
+    H = -np.sum(plogp)
+    return p, float(H), a, float(p[a])
+
+
+def canvas_sample(logits, E, entropy_bound: float, seed: int, step: int,
+                  temperature: float = 1.0, commit_mode: int = 0, canvas_len: Optional[int] = None,
+                  frozen=None, frozen_tokens=None, probs_storage: str = "fp64",
+                  soft_rows: Optional[Iterable[int]] = None):
+    """One sampler call over ``rows`` positions.
+
+    logits [rows, V] and E [V, D] are exact fp64 values.  Returns a dict with
+    tokens, commit_mask, entropy, confidence, argmax (per row), probs
+    [rows, V] (as stored: fp64 or bf16-rounded) and soft_emb [rows, D]
+    (NaN rows outside ``soft_rows`` when that is given).
+    """
+    logits = np.asarray(logits, np.float64)
+    rows, V = logits.shape
+    C = rows if canvas_len is None else int(canvas_len)
+    probs = np.empty((rows, V))
+    H = np.empty(rows)
+    conf = np.empty(rows)
+    amax = np.empty(rows, dtype=np.int64)
+    for r in range(rows):
+        p, h, a, c = row_statistics(logits[r], temperature)
+        probs[r], H[r], amax[r], conf[r] = p, h, a, c
+    frozen_m = np.zeros(rows, bool) if frozen is None else np.asarray(frozen).astype(bool)
+    below = H < entropy_bound
+    if commit_mode == 0:
+        commit = frozen_m | below
+    elif commit_mode == 1:
+        commit = np.zeros(rows, bool)
+        for r0 in range(0, rows, C):
+            for r in range(r0, min(r0 + C, rows)):
+                if frozen_m[r] or below[r]:
+                    commit[r] = True
+                else:
+                    break
+        commit |= frozen_m
+    else:
+        raise ValueError(commit_mode)
+    tokens = np.empty(rows, dtype=np.int64)
+    for r in range(rows):
+        if frozen_m[r]:
+            tokens[r] = int(frozen_tokens[r])
+        elif commit[r]:
+            tokens[r] = amax[r]
+        else:
+            tokens[r] = renoise_token(seed, step, r, V)
+    stored = bf16_round(probs) if probs_storage == "bf16" else probs
+    soft = None
+    if E is not None:
+        E = np.asarray(E, np.float64)
+        if soft_rows is None:
+            soft = stored @ E
+        else:
+            soft = np.full((rows, E.shape[1]), np.nan)
+            for r in soft_rows:
+                soft[r] = stored[r] @ E
+    return dict(tokens=tokens, commit_mask=commit.astype(np.uint8), entropy=H, confidence=conf,
+                argmax=amax, probs=stored, soft_emb=soft)

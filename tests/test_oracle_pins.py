@@ -1,0 +1,369 @@
+"""Pins of the fp64 oracle to facts outside itself (CPU only).
+
+Each test ties one oracle function to something the pages or mathematics fix:
+a hand expansion, a closed form, an invariant, a library routine, or a
+published test vector.  A plausible mistake in the oracle (dropped term, sign,
+index, transposed operand, off-by-one window) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import canvas_workloads as wl
+from oracle import attention as oatt
+from oracle import numerics as onum
+from oracle import sampler as osamp
+from oracle import splitmix as osm
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 rounding
+def test_bf16_round_matches_torch_and_workload_quantiser():
+    rng = np.random.default_rng(5)
+    a = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ours = onum.bf16_round(a.astype(np.float64))
+    lib = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(ours, lib)
+    wl_vals = wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(a)).astype(np.float64)
+    np.testing.assert_array_equal(wl_vals, lib)
+
+
+def test_bf16_round_ties_to_even():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 -> the even neighbour 1
+    assert onum.bf16_round(1.0 + 2.0 ** -8) == 1.0
+    # 1 + 3*2^-8 lies halfway between 1 + 2^-7 (odd) and 1 + 2^-6 (even)
+    assert onum.bf16_round(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert onum.bf16_round(-3.0) == -3.0
+
+
+# ---------------------------------------------------------------- rms
+def test_rms_hand_case():
+    # ||(3,4)|| = 5, sqrt(d) = sqrt(2)
+    got = onum.rms(np.array([3.0, 4.0]), 1.0, 0.0)
+    np.testing.assert_allclose(got, [3 * math.sqrt(2) / 5, 4 * math.sqrt(2) / 5], rtol=1e-15)
+    got = onum.rms(np.array([3.0, 4.0]), np.array([2.0, 0.5]), 1.0)
+    np.testing.assert_allclose(got, [2 * 3 * math.sqrt(2) / 6, 0.5 * 4 * math.sqrt(2) / 6], rtol=1e-15)
+
+
+def test_rms_norm_identity():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((7, 64)) * 3
+    g, eps = 1.7, 1e-3
+    y = onum.rms(x, np.full(64, g), eps)
+    nx = np.linalg.norm(x, axis=-1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), math.sqrt(64) * g * nx / (nx + eps), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_frequencies_closed_form():
+    np.testing.assert_allclose(onum.rope_frequencies(8, 1e4), [1.0, 0.1, 0.01, 0.001], rtol=1e-15)
+    f = onum.rope_frequencies(512, 1e6, 0.25)
+    assert np.count_nonzero(f) == 64 and f.shape == (256,)
+    assert f[63] == pytest.approx(1e6 ** (-126 / 512), rel=1e-14) and f[64] == 0.0
+    # the workload's fp32 table is the same spectrum, rounded to fp32
+    np.testing.assert_allclose(wl.rope_frequencies(512, 1e6, 0.25), f, rtol=1e-7)
+    np.testing.assert_allclose(wl.rope_frequencies(256, 1e4), onum.rope_frequencies(256, 1e4), rtol=1e-7)
+
+
+def test_rotate_equals_complex_rotation_of_split_half_pairs():
+    # an independent formulation: channel pair (t, t + d/2) as the complex
+    # number x_t + i x_{t+d/2}, multiplied by exp(i * angle)
+    rng = np.random.default_rng(2)
+    L, d, start = 5, 12, 7
+    x = rng.standard_normal((3, L, d))
+    freq = rng.uniform(0.0, 2.0, d // 2)
+    h = d // 2
+    z = (x[..., :h] + 1j * x[..., h:]) * np.exp(1j * (np.arange(L)[:, None] + start) * freq)
+    want = np.concatenate([z.real, z.imag], axis=-1)
+    np.testing.assert_allclose(onum.rotate(x, freq, start), want, rtol=1e-13, atol=1e-13)
+
+
+def test_rotate_hand_case_d4():
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    f = np.array([0.5, 0.25])
+    a0, a1 = 3 * 0.5, 3 * 0.25      # row 0 at position start=3
+    want = [math.cos(a0) * 1 - math.sin(a0) * 3, math.cos(a1) * 2 - math.sin(a1) * 4,
+            math.cos(a0) * 3 + math.sin(a0) * 1, math.cos(a1) * 4 + math.sin(a1) * 2]
+    np.testing.assert_allclose(onum.rotate(x, f, 3)[0], want, rtol=1e-15)
+
+
+def test_rotate_invariants():
+    rng = np.random.default_rng(3)
+    d = 16
+    f = onum.rope_frequencies(d, 1e4, 0.25)   # only 2 of 8 frequencies nonzero
+    x = rng.standard_normal((1, d))
+    y = onum.rotate(x, f, 123)
+    # zero-frequency channels come back unchanged
+    zero = np.concatenate([f, f]) == 0
+    np.testing.assert_array_equal(y[0, zero], x[0, zero])
+    # each (t, t + d/2) pair keeps its length
+    h = d // 2
+    np.testing.assert_allclose(np.hypot(y[0, :h], y[0, h:]), np.hypot(x[0, :h], x[0, h:]), rtol=1e-14)
+    # relative position: <rot(q, m), rot(k, n)> depends only on m - n
+    f = onum.rope_frequencies(d, 1e4)
+    q, k = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    s1 = onum.rotate(q, f, 10) @ onum.rotate(k, f, 3).T
+    s2 = onum.rotate(q, f, 1010) @ onum.rotate(k, f, 1003).T
+    np.testing.assert_allclose(s1, s2, rtol=1e-10)
+
+
+def test_logit_invariant_constant_gamma():
+    # with constant gamma, q.k = d * gq * gk * cos(theta) * |a|/(|a|+eps) * |b|/(|b|+eps)
+    rng = np.random.default_rng(4)
+    d, gq, gk, eps = 64, 1.3, 0.8, 1e-6
+    a, b = rng.standard_normal(d), rng.standard_normal(d)
+    q, k = onum.rms(a, np.full(d, gq), eps), onum.rms(b, np.full(d, gk), eps)
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    cos = a @ b / (na * nb)
+    want = d * gq * gk * cos * (na / (na + eps)) * (nb / (nb + eps))
+    assert q @ k == pytest.approx(want, rel=1e-12)
+    # rotating both at the same position leaves the logit unchanged
+    f = onum.rope_frequencies(d, 1e4)
+    assert (onum.rotate(q[None], f, 77) @ onum.rotate(k[None], f, 77).T)[0, 0] == pytest.approx(want, rel=1e-12)
+
+
+# ---------------------------------------------------------------- attention
+def _small_cfg(**kw):
+    base = dict(name="t", B=2, C=8, prefix=(40, 29), D=24, Hq=4, Hkv=2, d=16, layer="sliding",
+                window=16, theta=1e4, rotary_fraction=1.0, dtype="fp32", seed=9, gamma_q=1.1,
+                gamma_k=0.9, page_tokens=16)
+    base.update(kw)
+    return wl.AttnConfig(**base)
+
+
+def _f64(inp, name):
+    a = getattr(inp, name)
+    return None if a is None else wl.as_f64(a, inp.cfg.dtype)
+
+
+def _run_oracle(inp, storage="fp64", **kw):
+    c = inp.cfg
+    return oatt.canvas_attention(_f64(inp, "x"), _f64(inp, "W_q"), _f64(inp, "W_k"), _f64(inp, "W_v"),
+                                 c.Hq, c.Hkv, c.d, inp.gamma_q, inp.gamma_k, c.eps, inp.freq, c.layer,
+                                 _f64(inp, "cache_k"), _f64(inp, "cache_v"), inp.prefix_len, c.window,
+                                 storage=storage, **kw)
+
+
+def test_visible_pair_counts_match_workload_closed_forms():
+    # sliding workload: sum_i (1024 - i) + 256 * 256 = 295040 pairs per head
+    assert oatt.visible_pairs(256, 4096, 1024, "sliding") == 295040
+    assert oatt.visible_pairs(256, 32768, 0, "global") == 256 * 33024
+
+
+@pytest.mark.parametrize("layer", ["sliding", "global"])
+def test_uniform_attention_pins_the_visible_key_set(layer):
+    # gamma_q -> 0 makes every score 0: each output is the plain mean of the
+    # visible value rows.  Value rows carry (position, 1) in channels 0, 1 and
+    # the canvas values are 0 (W_v = 0 / canvas r = 0), so channel 0 gives the
+    # sum of visible prefix positions and channel 1 their count, over n + C.
+    cfg = _small_cfg(layer=layer, gamma_q=1e-30, window=16 if layer == "sliding" else 0)
+    inp = wl.make_attention_inputs(cfg)
+    P = cfg.max_prefix
+    ck = np.zeros((cfg.B, cfg.Hkv, P, cfg.d))
+    ck[..., 0] = np.arange(P)
+    ck[..., 1] = 1.0
+    x = _f64(inp, "x")
+    Wk = _f64(inp, "W_k")
+    if layer == "global":
+        Wk = np.zeros_like(Wk)      # canvas raw r = 0 -> canvas values 0
+        cache_v, Wv = None, None
+    else:
+        cache_v, Wv = ck, np.zeros_like(_f64(inp, "W_v"))
+        ck = np.random.default_rng(0).standard_normal(ck.shape)   # keys do not matter
+    out, _ = oatt.canvas_attention(x, _f64(inp, "W_q"), Wk, Wv, cfg.Hq, cfg.Hkv, cfg.d, inp.gamma_q,
+                                   inp.gamma_k, cfg.eps, inp.freq, layer, ck if layer == "global" else ck,
+                                   cache_v, inp.prefix_len, cfg.window)
+    if layer == "global":
+        # global values are the raw rows: channel 0 = position, channel 1 = 1
+        pass
+    for b in range(cfg.B):
+        Pb = int(inp.prefix_len[b])
+        for i in range(cfg.C):
+            lo = max(0, Pb + i - cfg.window) if (layer == "sliding" and cfg.window > 0) else 0
+            n = Pb - lo
+            for h in range(cfg.Hq):
+                o = out[b, i, h * cfg.d:(h + 1) * cfg.d]
+                assert o[1] == pytest.approx(n / (n + cfg.C), abs=1e-12)
+                assert o[0] == pytest.approx(sum(range(lo, Pb)) / (n + cfg.C), rel=1e-12, abs=1e-12)
+
+
+def test_single_key_returns_its_value_row_and_gqa_mapping():
+    # empty prefix and a one-token canvas: each query head sees exactly one key,
+    # so its output is the value row of KV head floor(h / G) -- the projection
+    # x W_v^T sliced by head.
+    cfg = _small_cfg(B=1, C=1, prefix=(0,), Hq=6, Hkv=2)
+    inp = wl.make_attention_inputs(cfg)
+    out, lse = _run_oracle(inp)
+    v = _f64(inp, "x")[0, 0] @ _f64(inp, "W_v").T
+    for h in range(6):
+        hk = h // 3
+        np.testing.assert_allclose(out[0, 0, h * 16:(h + 1) * 16], v[hk * 16:(hk + 1) * 16], rtol=1e-13)
+
+
+def _sdpa_reference(inp):
+    """The attention core through torch's scaled_dot_product_attention (fp64)
+    with an explicit boolean mask, fed with q/k/v assembled from the pinned
+    rms / rotate building blocks."""
+    c = inp.cfg
+    x, Wq, Wk = _f64(inp, "x"), _f64(inp, "W_q"), _f64(inp, "W_k")
+    Wv = _f64(inp, "W_v")
+    outs = []
+    for b in range(c.B):
+        P = int(inp.prefix_len[b])
+        q = (x[b] @ Wq.T).reshape(c.C, c.Hq, c.d).transpose(1, 0, 2)
+        k = (x[b] @ Wk.T).reshape(c.C, c.Hkv, c.d).transpose(1, 0, 2)
+        v = k if Wv is None else (x[b] @ Wv.T).reshape(c.C, c.Hkv, c.d).transpose(1, 0, 2)
+        q = onum.rotate(onum.rms(q, inp.gamma_q, c.eps), inp.freq, P)
+        if c.layer == "sliding":
+            K = np.concatenate([_f64(inp, "cache_k")[b, :, :P], onum.rotate(onum.rms(k, inp.gamma_k, c.eps), inp.freq, P)], 1)
+            Vv = np.concatenate([_f64(inp, "cache_v")[b, :, :P], v], 1)
+        else:
+            r = np.concatenate([_f64(inp, "cache_k")[b, :, :P], k], 1)
+            K = onum.rotate(onum.rms(r, inp.gamma_k, c.eps), inp.freq, 0)
+            Vv = r
+        mask = np.ones((c.C, P + c.C), bool)
+        if c.layer == "sliding" and c.window > 0:
+            for i in range(c.C):
+                mask[i, :max(0, P + i - c.window)] = False
+        G = c.Hq // c.Hkv
+        Kq = np.repeat(K, G, axis=0)
+        Vq = np.repeat(Vv, G, axis=0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(Kq), torch.from_numpy(Vq),
+            attn_mask=torch.from_numpy(mask), scale=1.0).numpy()
+        outs.append(o.transpose(1, 0, 2).reshape(c.C, c.Hq * c.d))
+    return np.stack(outs)
+
+
+@pytest.mark.parametrize("layer,window,rot", [("sliding", 16, 1.0), ("sliding", 0, 1.0), ("global", 0, 0.25)])
+def test_attention_matches_library_sdpa(layer, window, rot):
+    cfg = _small_cfg(layer=layer, window=window, rotary_fraction=rot, gamma_q=None, gamma_k=None,
+                     theta=1e6 if layer == "global" else 1e4)
+    inp = wl.make_attention_inputs(cfg)
+    out, _ = _run_oracle(inp)
+    np.testing.assert_allclose(out, _sdpa_reference(inp), rtol=1e-10, atol=1e-12)
+
+
+def test_global_storage_model_decomposition():
+    # rotate(rms(r, g)) == g * sqrt(d)/(|r|+eps) * rotate(r) for constant g; the
+    # bf16 storage model only inserts a rounding of rotate(r)
+    rng = np.random.default_rng(6)
+    d, eps, g = 32, 1e-6, 1.7
+    r = rng.standard_normal((9, d))
+    f = onum.rope_frequencies(d, 1e6, 0.25)
+    lhs = onum.rotate(onum.rms(r, np.full(d, g), eps), f, 5)
+    s = math.sqrt(d) / (np.linalg.norm(r, axis=-1, keepdims=True) + eps)
+    np.testing.assert_allclose(lhs, g * s * onum.rotate(r, f, 5), rtol=1e-13)
+    # and the two storage modes of the full layer agree to bf16 rounding level
+    cfg = _small_cfg(layer="global", window=0, rotary_fraction=0.25, theta=1e6, dtype="bf16")
+    inp = wl.make_attention_inputs(cfg)
+    a, _ = _run_oracle(inp, "fp64")
+    b, _ = _run_oracle(inp, "bf16")
+    assert np.max(np.abs(a - b)) < 0.05 and np.max(np.abs(a - b)) > 0
+
+
+def test_attention_row_subset_matches_full():
+    cfg = _small_cfg()
+    inp = wl.make_attention_inputs(cfg)
+    full, lse = _run_oracle(inp)
+    rows = [(0, 1, 3), (1, 3, 7)]
+    part, lse_p = _run_oracle(inp, rows=rows)
+    for (b, h, i) in rows:
+        np.testing.assert_array_equal(part[b, i, h * 16:(h + 1) * 16], full[b, i, h * 16:(h + 1) * 16])
+        assert lse_p[b, i, h] == lse[b, i, h]
+    assert np.isnan(part[0, 0, 0])
+
+
+# ---------------------------------------------------------------- sampler
+def test_entropy_extremes_and_two_level_closed_form():
+    V = 512
+    p, H, a, c = osamp.row_statistics(np.zeros(V))
+    assert H == pytest.approx(math.log(V), rel=1e-14) and a == 0 and c == pytest.approx(1 / V)
+    row = np.full(V, -1000.0)
+    row[17] = 0.0
+    p, H, a, c = osamp.row_statistics(row)
+    assert H == 0.0 and a == 17 and c == 1.0
+    # one logit A, n = V-1 logits Bv
+    A, Bv, n = 3.0, -0.5, V - 1
+    row = np.full(V, Bv)
+    row[100] = A
+    p1 = math.exp(A) / (math.exp(A) + n * math.exp(Bv))
+    q = math.exp(Bv) / (math.exp(A) + n * math.exp(Bv))
+    p, H, a, c = osamp.row_statistics(row)
+    assert H == pytest.approx(-p1 * math.log(p1) - n * q * math.log(q), rel=1e-13)
+    assert a == 100 and c == pytest.approx(p1, rel=1e-14)
+    # temperature 2 on logits 2*row is the same distribution
+    _, H2, _, _ = osamp.row_statistics(2 * row, temperature=2.0)
+    assert H2 == pytest.approx(H, rel=1e-13)
+
+
+def test_argmax_lowest_index_on_ties():
+    row = np.zeros(64)
+    row[[5, 9, 40]] = 2.0
+    assert osamp.row_statistics(row)[2] == 5
+
+
+def test_commit_renoise_rule_and_soft_embedding_closed_forms():
+    V, D, C = 64, 8, 4
+    rng = np.random.default_rng(8)
+    E = rng.standard_normal((V, D))
+    logits = np.zeros((8, V))              # uniform rows: H = ln 64 = 4.16
+    logits[1, 7] = 1e4                     # one-hot rows: H = 0
+    logits[2, 3] = 1e4
+    logits[6, 60] = 1e4
+    res = osamp.canvas_sample(logits, E, entropy_bound=0.5, seed=42, step=3, canvas_len=C)
+    np.testing.assert_array_equal(res["commit_mask"], [0, 1, 1, 0, 0, 0, 1, 0])
+    for r in range(8):
+        if res["commit_mask"][r]:
+            assert res["tokens"][r] == res["argmax"][r]
+        else:
+            assert res["tokens"][r] == osm.renoise_key(42, 3, r) % V
+    # one-hot P gives the E row exactly; uniform P gives the column means
+    np.testing.assert_array_equal(res["soft_emb"][1], E[7])
+    np.testing.assert_allclose(res["soft_emb"][0], E.mean(axis=0), rtol=1e-12, atol=1e-14)
+    # left-prefix mode: canvas 0 = rows 0..3 -> row 0 fails -> nothing committed;
+    # canvas 1 = rows 4..7 -> rows 4,5 fail -> nothing; make row 4 frozen
+    frozen = np.zeros(8, np.uint8)
+    frozen[4] = 1
+    ft = np.full(8, -1)
+    ft[4] = 11
+    res = osamp.canvas_sample(logits, E, 0.5, 42, 3, commit_mode=1, canvas_len=C, frozen=frozen,
+                              frozen_tokens=ft)
+    np.testing.assert_array_equal(res["commit_mask"], [0, 0, 0, 0, 1, 0, 0, 0])
+    assert res["tokens"][4] == 11
+    logits[5, 1] = 1e4
+    res = osamp.canvas_sample(logits, E, 0.5, 42, 3, commit_mode=1, canvas_len=C, frozen=frozen,
+                              frozen_tokens=ft)
+    np.testing.assert_array_equal(res["commit_mask"], [0, 0, 0, 0, 1, 1, 1, 0])
+    # strict bound: H equal to the bound does not commit
+    res = osamp.canvas_sample(np.zeros((1, V)), None, math.log(V), 0, 0)
+    assert res["commit_mask"][0] == 0
+
+
+# ---------------------------------------------------------------- splitmix64
+def test_splitmix64_published_vectors():
+    with open(os.path.join(GOLDEN, "splitmix64_vectors.txt")) as fh:
+        lines = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")]
+    for ln in lines:
+        seed, kind, n = int(ln[1]), ln[2], int(ln[3].rstrip(":"))
+        vals = [int(v) for v in ln[4:]]
+        if kind == "first":
+            assert osm.stream(seed, n) == vals
+        else:
+            bins = [0] * 5
+            for z in osm.stream(seed, n):
+                bins[(z * 5) >> 64] += 1
+            assert bins == vals
+
+
+def test_renoise_key_composition():
+    # key = mix(mix(mix(seed) ^ step) ^ row), mix = one SplitMix64 output
+    s0 = osm.stream(7, 1)[0]
+    s1 = osm.stream(s0 ^ 3, 1)[0]
+    s2 = osm.stream(s1 ^ 129, 1)[0]
+    assert osm.renoise_key(7, 3, 129) == s2
+    assert osm.renoise_token(7, 3, 129, 262144) == s2 & (262144 - 1)
