@@ -1,0 +1,451 @@
+"""Benchmark of one canvas refinement step on B300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+canvas_attention on the global-layer workload (batch 1, canvas 256, committed
+prefix 32768 in a paged bf16 cache, d_model 2816, 16 query / 2 KV heads,
+head_dim 512, shared W_v = W_k, partial RoPE) followed by canvas_sample on the
+full-vocab workload (256 positions x vocab 262144 bf16 logits, E 262144 x 2816
+bf16).  All inputs are seeded synthetic draws (canvas_workloads); no dataset or
+trained weights are involved.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own step on
+its own GPU (canvases are independent: weak scaling, no data-path
+collective); times are the max over ranks.  ``--impl reference`` times the
+fp64 CPU oracle (the reference arm of this tier) on bounded samples.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import canvas_workloads as wl  # noqa: E402
+
+METRIC = "canvas steps/sec (attn+sampler), attention TFLOP/s, sampler HBM GB/s"
+WORKLOAD = ("global-layer canvas step: canvas_attention B=1 C=256 prefix=32768 D=2816 Hq=16 Hkv=2 d=512 "
+            "(shared W_v=W_k, partial RoPE, paged bf16 cache, page 64) + canvas_sample rows=256 V=262144 "
+            "E=262144x2816 bf16")
+L2_BYTES = 126 * 1024 * 1024
+
+
+def attn_flops(cfg: wl.AttnConfig) -> float:
+    """Algorithmic attention FLOPs: 4 * d per visible (query, key) pair per head
+    (2d for Q.K, 2d for P.V); masked pairs and split-combine work not counted."""
+    pairs = 0
+    for P in cfg.prefix:
+        for i in range(cfg.C):
+            lo = 0 if (cfg.layer == "global" or cfg.window <= 0) else max(0, P + i - cfg.window)
+            pairs += (P - lo) + cfg.C
+    return 4.0 * cfg.d * cfg.Hq * pairs
+
+
+def sampler_bytes(s: wl.SampleConfig) -> float:
+    """Algorithmic bytes of the vocab reduction: read logits once, write the
+    bf16 probabilities once (plus per-row outputs)."""
+    return s.rows * s.V * 2 + s.rows * s.V * 2 + s.rows * 17
+
+
+def soft_emb_bytes(s: wl.SampleConfig) -> float:
+    """Algorithmic bytes of P.E: read E and P once, write fp32 soft_emb once."""
+    return s.V * s.D * 2 + s.rows * s.V * 2 + s.rows * s.D * 4
+
+
+def soft_emb_flops(s: wl.SampleConfig) -> float:
+    return 2.0 * s.rows * s.V * s.D
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = f"/tmp/canvas_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+class Step:
+    """Device state of one canvas step (attention + sampler)."""
+
+    def __init__(self, device):
+        import torch
+        import canvas_denoising_step_03_b300 as cv
+        self.cv, self.torch = cv, torch
+        self.acfg, self.scfg = wl.GLOBAL, wl.FULL_SAMPLE
+        a = wl.make_attention_inputs(self.acfg)
+        s = wl.make_sample_inputs(self.scfg)
+        self.a_in, self.s_in = a, s
+        dev = device
+
+        def d16(x):
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        c = self.acfg
+        self.x = d16(a.x)
+        self.W_q, self.W_k = d16(a.W_q), d16(a.W_k)
+        self.gq = torch.from_numpy(a.gamma_q).to(dev)
+        self.gk = torch.from_numpy(a.gamma_k).to(dev)
+        self.freq = torch.from_numpy(a.freq).to(dev)
+        table, npages = wl.page_layout(c)
+        self.table = torch.from_numpy(table).to(dev)
+        self.pool = d16(wl.scatter_pages(a.cache_k, table, npages, c.page_tokens))
+        self.kv = cv.make_kv_cache(self.pool, None, self.table, c.page_tokens)
+        self.prefix = torch.from_numpy(a.prefix_len).to(dev)
+        self.out = torch.empty((c.B, c.C, c.Hq * c.d), dtype=torch.bfloat16, device=dev)
+        self.aws = cv.workspace(cv.canvas_attention_workspace_size(cv.CANVAS_BF16, c.B, c.C, c.D, c.Hq, c.Hkv, c.d,
+                                                                   c.max_prefix, cv.CANVAS_LAYER_GLOBAL), dev)
+        sc = self.scfg
+        self.logits = d16(s.logits)
+        self.E = d16(s.E)
+        R = sc.rows
+        self.tokens = torch.empty(R, dtype=torch.int32, device=dev)
+        self.mask = torch.empty(R, dtype=torch.uint8, device=dev)
+        self.ent = torch.empty(R, dtype=torch.float32, device=dev)
+        self.conf = torch.empty(R, dtype=torch.float32, device=dev)
+        self.soft = torch.empty((R, sc.D), dtype=torch.float32, device=dev)
+        self.sws = cv.workspace(cv.canvas_sample_workspace_size(cv.CANVAS_BF16, R, sc.V, sc.D), dev)
+        self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def run(self, step_idx: int = 0, x=None, logits=None):
+        cv, c, sc = self.cv, self.acfg, self.scfg
+        cv.canvas_attention(self.x if x is None else x, self.W_q, self.W_k, None, c.Hq, c.Hkv, c.d, self.gq,
+                            self.gk, c.eps, self.freq, cv.CANVAS_LAYER_GLOBAL, self.kv, self.prefix, c.max_prefix,
+                            0, 1.0, 0, self.out, None, self.aws)
+        cv.canvas_sample(self.logits if logits is None else logits, self.E, sc.bound, sc.seed, step_idx, 1.0, 0,
+                         sc.C, None, None, self.tokens, self.mask, self.ent, self.conf, None, None, cv.CANVAS_BF16,
+                         self.soft, self.sws)
+
+    def flush_l2(self):
+        self.flush.fill_(1.0)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import canvas_denoising_step_03_b300 as cv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    st = Step(dev)
+    stream = torch.cuda.current_stream()
+    ids = [cv.CANVAS_KERNEL_PREP, cv.CANVAS_KERNEL_ATTENTION, cv.CANVAS_KERNEL_SAMPLER, cv.CANVAS_KERNEL_SOFT_EMB]
+    names = {cv.CANVAS_KERNEL_PREP: "attention_prep", cv.CANVAS_KERNEL_ATTENTION: "attention_core",
+             cv.CANVAS_KERNEL_SAMPLER: "sampler", cv.CANVAS_KERNEL_SOFT_EMB: "soft_emb_gemm"}
+
+    for w in range(args.warmup):
+        st.flush_l2()
+        st.run(w)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+
+    # per-step, per-kernel events
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ids]
+          for _ in range(args.steps)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for row in ev:  # materialise the event handles
+        for a, b in row:
+            a.record(); b.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = cv.canvas_kernel_launches()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        st.flush_l2()  # outside the step's events
+        for kid, (a, b) in zip(ids, ev[k]):
+            cv.canvas_profile_events(kid, a, b)
+        step_ev[k][0].record(stream)
+        st.run(args.warmup + k)
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    launches = cv.canvas_kernel_launches() - launches0
+    clk = clocks.stop()
+    for kid in ids:
+        cv.canvas_profile_events(kid, None, None)
+    if world > 1:
+        dist.barrier()
+    status = cv.canvas_device_status()
+    assert status == cv.CANVAS_OK, cv.canvas_last_error()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    kern_ms = {names[kid]: statistics.mean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+               for j, kid in enumerate(ids)}
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host inputs (pinned) -> device, results -> host, every step
+    x_h = torch.empty(st.x.shape, dtype=torch.bfloat16).pin_memory()
+    lg_h = torch.empty(st.logits.shape, dtype=torch.bfloat16).pin_memory()
+    x_h.copy_(st.x.cpu())
+    lg_h.copy_(st.logits.cpu())
+    x_d = torch.empty_like(st.x)
+    lg_d = torch.empty_like(st.logits)
+    outs = [st.out, st.tokens, st.mask, st.ent, st.conf, st.soft]
+    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = x_h.numel() * 2 + lg_h.numel() * 2
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for w in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        st.run(w, x_d, lg_d)
+        for o, oh in zip(outs, outs_h):
+            oh.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    for k in range(args.steps):
+        st.flush_l2()
+        e2e_ev[k][0].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        st.run(k, x_d, lg_d)
+        for o, oh in zip(outs, outs_h):
+            oh.copy_(o, non_blocking=True)
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert cv.canvas_device_status() == cv.CANVAS_OK
+
+    if rank != 0:
+        return None
+    hbm, bf16, peak_src = measured_peaks()
+    af = attn_flops(st.acfg)
+    att_tflops = af / (kern_ms["attention_core"] * 1e-3) / 1e12
+    samp_gbs = sampler_bytes(st.scfg) / (kern_ms["sampler"] * 1e-3) / 1e9
+    se_gbs = soft_emb_bytes(st.scfg) / (kern_ms["soft_emb_gemm"] * 1e-3) / 1e9
+    dominant = max(("attention_core", "soft_emb_gemm", "sampler"), key=lambda n: kern_ms[n])
+    if dominant == "attention_core":
+        roof = {"kernel": "attention_core", "bound": "tensor", "achieved": round(att_tflops, 2), "peak": bf16,
+                "unit": "TFLOP/s", "frac": round(att_tflops / bf16, 4),
+                "algorithmic": f"{af:.4g} FLOP per launch (4*d per visible query-key pair per head)"}
+    elif dominant == "soft_emb_gemm":
+        roof = {"kernel": "soft_emb_gemm", "bound": "hbm", "achieved": round(se_gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(se_gbs / hbm, 4),
+                "algorithmic": f"{soft_emb_bytes(st.scfg):.4g} B per launch (E + P read once, soft_emb written)"}
+    else:
+        roof = {"kernel": "sampler", "bound": "hbm", "achieved": round(samp_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(samp_gbs / hbm, 4),
+                "algorithmic": f"{sampler_bytes(st.scfg):.4g} B per launch (logits read, bf16 probs written)"}
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'}, burst)"
+    roof["traffic"] = load_traffic(roof["kernel"])
+    line = {
+        "metric": METRIC,
+        "value": round(world * 1000.0 / ms, 3),
+        "unit": "canvas steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded draws; random weights and caches; no dataset)",
+        "config": {"workload": WORKLOAD, "l2": "flushed between timed steps (252 MB write, outside the step events)",
+                   "parallelism": f"replicas x{world} (independent canvases per GPU)"},
+        "attention_tflops": round(att_tflops, 2),
+        "sampler_hbm_gbs": round(samp_gbs, 1),
+        "soft_emb_hbm_gbs": round(se_gbs, 1),
+        "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+        "roofline": roof,
+        "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "canvas steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(st.a_in, st.s_in)
+    return line
+
+
+def load_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary of this kernel, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    return d.get(kernel)
+
+
+# --------------------------------------------------------------------------- oracle timings
+def oracle_step_sample(a_in, s_in, attn_rows, samp_rows, E64_chunks=16384):
+    """Time the fp64 oracle on a bounded sample of one step; returns (extrapolated
+    seconds per full step, description)."""
+    from oracle import attention as oatt
+    from oracle import sampler as osamp
+    c = a_in.cfg
+    f = lambda x: None if x is None else wl.as_f64(x, c.dtype)  # noqa: E731
+    t0 = time.perf_counter()
+    oatt.canvas_attention(f(a_in.x), f(a_in.W_q), f(a_in.W_k), None, c.Hq, c.Hkv, c.d,
+                          a_in.gamma_q.astype(np.float64), a_in.gamma_k.astype(np.float64), c.eps,
+                          a_in.freq.astype(np.float64), c.layer, f(a_in.cache_k), None, a_in.prefix_len, c.window,
+                          storage="bf16", rows=[(0, 0, 0)])
+    t_fixed = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oatt.canvas_attention(f(a_in.x), f(a_in.W_q), f(a_in.W_k), None, c.Hq, c.Hkv, c.d,
+                          a_in.gamma_q.astype(np.float64), a_in.gamma_k.astype(np.float64), c.eps,
+                          a_in.freq.astype(np.float64), c.layer, f(a_in.cache_k), None, a_in.prefix_len, c.window,
+                          storage="bf16", rows=attn_rows)
+    t_rows = time.perf_counter() - t0 - t_fixed
+    per_row = max(t_rows, 0.0) / max(1, len(attn_rows) - 0)
+    sc = s_in.cfg
+    t0 = time.perf_counter()
+    lg = wl.as_f64(s_in.logits[samp_rows], "bf16")
+    res = osamp.canvas_sample(lg, None, sc.bound, sc.seed, 0, canvas_len=sc.C, probs_storage="bf16")
+    soft = np.zeros((len(samp_rows), sc.D))
+    for v0 in range(0, sc.V, E64_chunks):
+        soft += res["probs"][:, v0:v0 + E64_chunks] @ wl.as_f64(s_in.E[v0:v0 + E64_chunks], "bf16")
+    t_samp = time.perf_counter() - t0
+    total_rows = c.B * c.C * c.Hq
+    t_full = t_fixed + per_row * total_rows + t_samp / len(samp_rows) * sc.rows
+    desc = (f"fp64 numpy oracle: attention fixed part (projections, all key transforms) + {len(attn_rows)} of "
+            f"{total_rows} query rows, sampler + soft embedding for {len(samp_rows)} of {sc.rows} positions; "
+            f"full step extrapolated linearly in rows")
+    return t_full, desc, t_fixed + t_rows + t_samp
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max((i.get("num_threads", 1) for i in info), default=1)
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(a_in, s_in):
+    attn_rows = [(0, h, i) for h in (0, 9) for i in (0, 255)]
+    t_full, desc, spent = oracle_step_sample(a_in, s_in, attn_rows, [0, 1])
+    return {"value": round(1.0 / t_full, 6), "unit": "canvas steps/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": desc, "cpu_seconds_spent": round(spent, 2),
+            "host_cpus": len(os.sched_getaffinity(0))}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    a_in = wl.make_attention_inputs(wl.GLOBAL)
+    s_in = wl.make_sample_inputs(wl.FULL_SAMPLE)
+    times = []
+    desc = ""
+    for k in range(args.warmup + args.steps):
+        t_full, desc, _ = oracle_step_sample(a_in, s_in, [(0, k % 16, (37 * k) % 256)], [k % 256])
+        if k >= args.warmup:
+            times.append(t_full)
+    ms = statistics.mean(times) * 1000.0
+    v = round(1000.0 / ms, 6)
+    cores = blas_threads()
+    return {"metric": METRIC, "value": v, "unit": "canvas steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded draws)", "impl": "reference",
+            "config": {"workload": WORKLOAD}, "cpu_baseline": {"value": v, "unit": "canvas steps/s", "cores": cores,
+                                                              "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "canvas steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

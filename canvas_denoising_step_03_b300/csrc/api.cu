@@ -1,0 +1,507 @@
+// api.cu -- the C ABI of libcanvas.so (declared in include/canvas.h):
+// argument validation, workspace layout, tensor-map encoding and the launch
+// sequence of each call.  No call allocates device memory or synchronises
+// (except canvas_device_status).
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace canvas {
+
+__device__ int g_status = 0;
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string t_last_error;
+
+// per-thread timing events (canvas_profile_events)
+struct EventPair {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+thread_local EventPair t_events[CANVAS_KERNEL_COUNT];
+
+inline void mark_start(int id, cudaStream_t s) {
+  if (t_events[id].start) cudaEventRecord(t_events[id].start, s);
+}
+inline void mark_stop(int id, cudaStream_t s) {
+  if (t_events[id].stop) cudaEventRecord(t_events[id].stop, s);
+}
+
+canvas_status fail(canvas_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+canvas_status fail(canvas_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+canvas_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(CANVAS_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define CANVAS_CUDA(call)                                   \
+  do {                                                      \
+    cudaError_t e_ = (call);                                \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);     \
+  } while (0)
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Carves a caller-owned workspace into aligned regions.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* p) : base(static_cast<char*>(p)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = align_up(off + bytes);
+    return p;
+  }
+};
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows][cols] (cols contiguous), box {box_cols, box_rows},
+// 128-byte swizzle, zero fill outside the tensor.
+canvas_status make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                            uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0)
+    return fail(CANVAS_ERR_ARG, "tensor base address must be 16-byte aligned");
+  if ((cols * 2) % 16 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "row pitch must be a multiple of 16 bytes");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return CANVAS_OK;
+}
+
+// ------------------------------------------------------------------ GEMM plan
+struct GemmPlan {
+  int m_tiles, n_tiles, kblocks, splits, two_acc;
+  size_t partial_bytes, counter_bytes;
+};
+
+constexpr int kNumSms = 148;
+
+GemmPlan plan_gemm(int M, int N, int K) {
+  GemmPlan p;
+  p.two_acc = M > kGemmBM ? 1 : 0;
+  p.m_tiles = (M + 255) / 256;
+  p.n_tiles = (N + kGemmBN - 1) / kGemmBN;
+  p.kblocks = (K + kGemmBK - 1) / kGemmBK;
+  const int tiles = p.m_tiles * p.n_tiles;
+  int s = tiles >= kNumSms ? 1 : kNumSms / tiles;
+  s = std::min(s, std::max(1, p.kblocks / 2));
+  p.splits = std::max(1, s);
+  p.partial_bytes = p.splits > 1 ? size_t(p.splits) * M * N * sizeof(float) : 0;
+  p.counter_bytes = size_t(tiles) * sizeof(int);
+  return p;
+}
+
+size_t gemm_ws_bytes(const GemmPlan& p) { return align_up(p.partial_bytes) + align_up(p.counter_bytes); }
+
+// C[M,N] = A[M,K] op(B) on the tensor cores; ws holds partials + counters.
+canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C, int M, int N, int K,
+                          int accumulate, void* ws, cudaStream_t stream) {
+  const GemmPlan p = plan_gemm(M, N, K);
+  CUtensorMap tmA, tmB;
+  canvas_status st = make_map_bf16(&tmA, A, M, K, kGemmBM, kGemmBK);
+  if (st != CANVAS_OK) return st;
+  if (b_mn_major)
+    st = make_map_bf16(&tmB, B, K, N, 64, 64);
+  else
+    st = make_map_bf16(&tmB, B, N, K, kGemmBN, kGemmBK);
+  if (st != CANVAS_OK) return st;
+  Carver cv(ws);
+  GemmTcArgs g;
+  g.partials = cv.take<float>(p.partial_bytes);
+  g.counters = cv.take<int>(p.counter_bytes);
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.ldc = N;
+  g.accumulate = accumulate;
+  g.b_mn_major = b_mn_major;
+  g.two_acc = p.two_acc;
+  g.m_tiles = p.m_tiles;
+  g.n_tiles = p.n_tiles;
+  g.splits = p.splits;
+  g.kblocks = p.kblocks;
+  if (p.splits > 1) CANVAS_CUDA(cudaMemsetAsync(g.counters, 0, p.counter_bytes, stream));
+  CANVAS_CUDA(launch_gemm_tc(tmA, tmB, g, stream));
+  return CANVAS_OK;
+}
+
+// ------------------------------------------------------------------ attention layout
+struct AttnLayout {
+  size_t proj_q, proj_k, proj_v, gemm, qp, kc, vc, kt, ks, vs, total;
+};
+
+AttnLayout attn_layout(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix, int layer_type) {
+  AttnLayout L;
+  const size_t M = size_t(B) * C;
+  const size_t es = dtype == CANVAS_BF16 ? 2 : 4;
+  const bool global = layer_type == CANVAS_LAYER_GLOBAL;
+  L.proj_q = M * Hq * d * 4;
+  L.proj_k = M * Hkv * d * 4;
+  L.proj_v = global ? 0 : M * Hkv * d * 4;
+  L.gemm = 0;
+  if (dtype == CANVAS_BF16) {
+    L.gemm = std::max(gemm_ws_bytes(plan_gemm(int(M), Hq * d, D)), gemm_ws_bytes(plan_gemm(int(M), Hkv * d, D)));
+  }
+  L.qp = M * Hq * d * es;
+  L.kc = M * Hkv * d * es;
+  L.vc = global ? 0 : M * Hkv * d * es;
+  const size_t Lk = size_t(max_prefix) + C;
+  L.kt = global ? size_t(B) * Hkv * Lk * d * es : 0;
+  L.ks = global ? size_t(B) * Hkv * Lk * 4 : 0;
+  L.vs = L.ks;
+  L.total = align_up(L.proj_q) + align_up(L.proj_k) + align_up(L.proj_v) + align_up(L.gemm) + align_up(L.qp) +
+            align_up(L.kc) + align_up(L.vc) + align_up(L.kt) + align_up(L.ks) + align_up(L.vs) + kAlign;
+  return L;
+}
+
+bool attn_shape_ok(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix, int layer_type) {
+  if (dtype != CANVAS_BF16 && dtype != CANVAS_FP32) return false;
+  if (B < 1 || C < 1 || D < 1 || Hq < 1 || Hkv < 1 || d < 2 || max_prefix < 0) return false;
+  if (Hq % Hkv != 0 || Hq / Hkv > 32) return false;
+  if (layer_type != CANVAS_LAYER_SLIDING && layer_type != CANVAS_LAYER_GLOBAL) return false;
+  return true;
+}
+
+// ------------------------------------------------------------------ sampler layout
+struct SampleLayout {
+  size_t probs, argmax, gemm, total;
+};
+
+SampleLayout sample_layout(int dtype, int rows, int V, int D) {
+  SampleLayout L;
+  L.probs = size_t(rows) * V * (dtype == CANVAS_BF16 ? 2 : 4);
+  L.argmax = size_t(rows) * 4;
+  L.gemm = dtype == CANVAS_BF16 ? gemm_ws_bytes(plan_gemm(rows, D, V)) : 0;
+  L.total = align_up(L.probs) + align_up(L.argmax) + align_up(L.gemm) + kAlign;
+  return L;
+}
+
+bool ws_ok(const void* ws, size_t have, size_t need) {
+  return ws != nullptr && have >= need && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0;
+}
+
+}  // namespace
+}  // namespace canvas
+
+using namespace canvas;
+
+extern "C" {
+
+const char* canvas_version(void) { return "canvas 0.1 (sm_103a)"; }
+
+const char* canvas_last_error(void) { return t_last_error.c_str(); }
+
+canvas_status canvas_profile_events(int kernel_id, void* start_event, void* stop_event) {
+  if (kernel_id < 0 || kernel_id >= CANVAS_KERNEL_COUNT) return fail(CANVAS_ERR_ARG, "canvas_profile_events: kernel id");
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(CANVAS_ERR_ARG, "canvas_profile_events: pass both events or neither");
+  t_events[kernel_id].start = static_cast<cudaEvent_t>(start_event);
+  t_events[kernel_id].stop = static_cast<cudaEvent_t>(stop_event);
+  return CANVAS_OK;
+}
+
+uint64_t canvas_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+canvas_status canvas_device_status(canvas_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(status)");
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(status)");
+    return fail(canvas_status(v), "device status %d recorded by a kernel", v);
+  }
+  return CANVAS_OK;
+}
+
+size_t canvas_gemm_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 1) return 0;
+  return gemm_ws_bytes(plan_gemm(M, N, K)) + kAlign;
+}
+
+canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float* C, int M, int N, int K,
+                               int accumulate, void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: null pointer");
+  if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: bad shape");
+  if (b_layout != 0 && b_layout != 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: b_layout must be 0 or 1");
+  if (K % 8 != 0 || N % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16: K and N must be multiples of 8");
+  if (!ws_ok(workspace, ws_bytes, canvas_gemm_workspace_size(M, N, K)))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_gemm_bf16: workspace missing, small or misaligned");
+  return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix,
+                                       int layer_type) {
+  if (!attn_shape_ok(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type)) return 0;
+  return attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type).total;
+}
+
+canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, const void* W_q, const void* W_k,
+                               const void* W_v, int Hq, int Hkv, int d, const float* gamma_q, const float* gamma_k,
+                               float eps, const float* freq, int layer_type, const canvas_kv_cache* kv,
+                               const int32_t* prefix_len, int max_prefix, int window, float scale, int v_unit_rms,
+                               void* out, float* lse, void* workspace, size_t ws_bytes, canvas_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!attn_shape_ok(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type))
+    return fail(CANVAS_ERR_ARG, "canvas_attention: invalid shape or dtype");
+  const bool global = layer_type == CANVAS_LAYER_GLOBAL;
+  const bool bf16 = dtype == CANVAS_BF16;
+  if (!x || !W_q || !W_k || !gamma_q || !gamma_k || !freq || !kv || !prefix_len || !out)
+    return fail(CANVAS_ERR_ARG, "canvas_attention: null pointer");
+  if (global && W_v != nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: global layers share W_v = W_k (pass NULL)");
+  if (!global && W_v == nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: sliding layers need W_v");
+  if (v_unit_rms && !global) return fail(CANVAS_ERR_ARG, "canvas_attention: v_unit_rms applies to global layers");
+  if (max_prefix > 0 && (!kv->k_pool || !kv->block_table)) return fail(CANVAS_ERR_ARG, "canvas_attention: cache pointers");
+  if (max_prefix > 0 && !global && !kv->v_pool) return fail(CANVAS_ERR_ARG, "canvas_attention: sliding cache needs v_pool");
+  if (global && kv->v_pool) return fail(CANVAS_ERR_ARG, "canvas_attention: global cache has no v_pool");
+  if (max_prefix > 0 && (kv->page_tokens < 1 || kv->num_pages < 1 ||
+                         (long long)kv->max_pages_per_seq * kv->page_tokens < max_prefix))
+    return fail(CANVAS_ERR_ARG, "canvas_attention: cache geometry cannot hold max_prefix tokens");
+  if (d % 64 != 0 || d > 512) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: head_dim must be 64, 128, ..., 512");
+  if (bf16 && D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: d_model must be a multiple of 8");
+  const AttnLayout L = attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type);
+  if (!ws_ok(workspace, ws_bytes, L.total))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_attention: workspace missing, small or misaligned (need %zu)", L.total);
+
+  Carver cv(workspace);
+  float* proj_q = cv.take<float>(L.proj_q);
+  float* proj_k = cv.take<float>(L.proj_k);
+  float* proj_v = cv.take<float>(L.proj_v);
+  void* gws = cv.take<char>(L.gemm);
+  void* Qp = cv.take<char>(L.qp);
+  void* Kc = cv.take<char>(L.kc);
+  void* Vc = cv.take<char>(L.vc);
+  void* Kt = cv.take<char>(L.kt);
+  float* ks = cv.take<float>(L.ks);
+  float* vs = cv.take<float>(L.vs);
+  const int M = B * C;
+
+  // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
+  mark_start(CANVAS_KERNEL_PREP, stream);
+  if (bf16) {
+    canvas_status st = run_gemm_tc(x, W_q, 0, proj_q, M, Hq * d, D, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+    st = run_gemm_tc(x, W_k, 0, proj_k, M, Hkv * d, D, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+    if (!global) {
+      st = run_gemm_tc(x, W_v, 0, proj_v, M, Hkv * d, D, 0, gws, stream);
+      if (st != CANVAS_OK) return st;
+    }
+  } else {
+    CANVAS_CUDA(launch_gemm_simt(x, W_q, 0, false, proj_q, M, Hq * d, D, 0, stream));
+    CANVAS_CUDA(launch_gemm_simt(x, W_k, 0, false, proj_k, M, Hkv * d, D, 0, stream));
+    if (!global) CANVAS_CUDA(launch_gemm_simt(x, W_v, 0, false, proj_v, M, Hkv * d, D, 0, stream));
+  }
+  // 2. rms + rotate of the canvas rows
+  PrologueArgs p;
+  p.proj_q = proj_q;
+  p.proj_k = proj_k;
+  p.proj_v = global ? nullptr : proj_v;
+  p.gamma_q = gamma_q;
+  p.gamma_k = gamma_k;
+  p.freq = freq;
+  p.prefix_len = prefix_len;
+  p.B = B;
+  p.C = C;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.d = d;
+  p.eps = eps;
+  p.global = global ? 1 : 0;
+  p.Qp = Qp;
+  p.Kc = Kc;
+  p.Vc = Vc;
+  CANVAS_CUDA(launch_prologue(p, bf16, stream));
+  // 3. global layers: rotated raw rows + norm scalars of every key
+  if (global) {
+    KeyPrepArgs k;
+    k.pool = kv->k_pool;
+    k.block_table = kv->block_table;
+    k.max_pages = kv->max_pages_per_seq;
+    k.page_tokens = kv->page_tokens;
+    k.num_pages = kv->num_pages;
+    k.Rc = Kc;
+    k.gamma_k = gamma_k;
+    k.freq = freq;
+    k.prefix_len = prefix_len;
+    k.B = B;
+    k.C = C;
+    k.Hkv = Hkv;
+    k.d = d;
+    k.max_prefix = max_prefix;
+    k.eps = eps;
+    k.Kt = Kt;
+    k.ks = ks;
+    k.vs = vs;
+    CANVAS_CUDA(launch_key_prep(k, bf16, stream));
+  }
+  mark_stop(CANVAS_KERNEL_PREP, stream);
+  // 4. attention
+  AttnArgs a;
+  a.Qp = Qp;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.block_table = kv->block_table;
+  a.max_pages = kv->max_pages_per_seq;
+  a.page_tokens = kv->page_tokens;
+  a.num_pages = kv->num_pages;
+  a.Kc = Kc;
+  a.Vc = Vc;
+  a.Kt = Kt;
+  a.ks = ks;
+  a.vs = vs;
+  a.prefix_len = prefix_len;
+  a.B = B;
+  a.C = C;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.max_prefix = max_prefix;
+  a.window = window;
+  a.global = global ? 1 : 0;
+  a.v_unit_rms = v_unit_rms ? 1 : 0;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  mark_start(CANVAS_KERNEL_ATTENTION, stream);
+  CANVAS_CUDA(launch_attention_simt(a, bf16, stream));
+  mark_stop(CANVAS_KERNEL_ATTENTION, stream);
+  return CANVAS_OK;
+}
+
+size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D) {
+  if ((dtype != CANVAS_BF16 && dtype != CANVAS_FP32) || rows < 1 || V < 1 || D < 1) return 0;
+  return sample_layout(dtype, rows, V, D).total;
+}
+
+canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, const void* E, int D,
+                            float entropy_bound, uint64_t seed, uint32_t step, float temperature, int commit_mode,
+                            int canvas_len, const uint8_t* frozen, const int32_t* frozen_tokens, int32_t* tokens,
+                            uint8_t* commit_mask, float* entropy, float* confidence, int32_t* argmax,
+                            void* probs_out, int probs_dtype, float* soft_emb, void* workspace, size_t ws_bytes,
+                            canvas_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype != CANVAS_BF16 && dtype != CANVAS_FP32) return fail(CANVAS_ERR_ARG, "canvas_sample: dtype");
+  if (rows < 1 || V < 1 || D < 1) return fail(CANVAS_ERR_ARG, "canvas_sample: bad shape");
+  if (!logits || !E || !tokens || !commit_mask || !entropy || !confidence || !soft_emb)
+    return fail(CANVAS_ERR_ARG, "canvas_sample: null pointer");
+  if ((frozen == nullptr) != (frozen_tokens == nullptr))
+    return fail(CANVAS_ERR_ARG, "canvas_sample: frozen and frozen_tokens go together");
+  if (!(temperature > 0.f)) return fail(CANVAS_ERR_ARG, "canvas_sample: temperature must be > 0");
+  if (commit_mode != 0 && commit_mode != 1) return fail(CANVAS_ERR_ARG, "canvas_sample: commit_mode");
+  if (canvas_len < 1 || (commit_mode == 1 && rows % canvas_len != 0))
+    return fail(CANVAS_ERR_ARG, "canvas_sample: canvas_len");
+  if (probs_out && probs_dtype != CANVAS_BF16 && probs_dtype != CANVAS_FP32)
+    return fail(CANVAS_ERR_ARG, "canvas_sample: probs_dtype");
+  if (V % 8 != 0 || D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_sample: V and D must be multiples of 8");
+  const SampleLayout L = sample_layout(dtype, rows, V, D);
+  if (!ws_ok(workspace, ws_bytes, L.total))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_sample: workspace missing, small or misaligned (need %zu)", L.total);
+  Carver cv(workspace);
+  char* probs_ws = cv.take<char>(L.probs);
+  int32_t* argmax_ws = cv.take<int32_t>(L.argmax);
+  void* gws = cv.take<char>(L.gemm);
+  const bool bf16 = dtype == CANVAS_BF16;
+
+  SampleArgs a;
+  a.rows = rows;
+  a.V = V;
+  // cluster of up to 8 CTAs per row; each CTA owns a multiple of 8 columns
+  int cl = 1;
+  while (cl < kMaxSampleCluster && (long long)V / (cl * 2) >= 4096) cl *= 2;
+  a.cluster = cl;
+  a.chunk = ((V + cl - 1) / cl + 7) / 8 * 8;
+  a.inv_temp = 1.0f / temperature;
+  a.bound = entropy_bound;
+  a.seed = seed;
+  a.step = step;
+  a.commit_mode = commit_mode;
+  a.canvas_len = canvas_len;
+  a.frozen = frozen;
+  a.frozen_tokens = frozen_tokens;
+  a.tokens = tokens;
+  a.commit_mask = commit_mask;
+  a.entropy = entropy;
+  a.confidence = confidence;
+  a.argmax = argmax ? argmax : argmax_ws;
+  // the probabilities the soft embedding multiplies: bf16 for bf16 calls,
+  // fp32 for fp32 calls; written to probs_out when its dtype matches
+  a.probs_bf16 = nullptr;
+  a.probs_f32 = nullptr;
+  if (bf16) {
+    a.probs_bf16 = (probs_out && probs_dtype == CANVAS_BF16) ? static_cast<__nv_bfloat16*>(probs_out)
+                                                              : reinterpret_cast<__nv_bfloat16*>(probs_ws);
+    if (probs_out && probs_dtype == CANVAS_FP32) a.probs_f32 = static_cast<float*>(probs_out);
+  } else {
+    a.probs_f32 = (probs_out && probs_dtype == CANVAS_FP32) ? static_cast<float*>(probs_out)
+                                                             : reinterpret_cast<float*>(probs_ws);
+    if (probs_out && probs_dtype == CANVAS_BF16) a.probs_bf16 = static_cast<__nv_bfloat16*>(probs_out);
+  }
+  mark_start(CANVAS_KERNEL_SAMPLER, stream);
+  CANVAS_CUDA(launch_sampler(a, logits, bf16, stream));
+  mark_stop(CANVAS_KERNEL_SAMPLER, stream);
+  // soft embedding P . E
+  mark_start(CANVAS_KERNEL_SOFT_EMB, stream);
+  if (bf16) {
+    const canvas_status st = run_gemm_tc(a.probs_bf16, E, 1, soft_emb, rows, D, V, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+  } else {
+    CANVAS_CUDA(launch_gemm_simt(a.probs_f32, E, 1, false, soft_emb, rows, D, V, 0, stream));
+  }
+  mark_stop(CANVAS_KERNEL_SOFT_EMB, stream);
+  return CANVAS_OK;
+}
+
+}  // extern "C"

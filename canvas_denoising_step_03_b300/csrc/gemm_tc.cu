@@ -1,0 +1,238 @@
+// gemm_tc.cu -- bf16 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+//   C[M,N] (fp32) = A[M,K] * op(B),   A row-major (K contiguous),
+//   B either [N,K] (K contiguous, "weights": C = A B^T, the pages' x @ W.T) or
+//   [K,N] (N contiguous: the embedding table in the soft embedding P.E).
+//
+// Used for the QKV projection of the attention layer and the soft embedding
+// P.E of the sampler (self-conditioning, AI Trends summary of a DiffusionGemma
+// 26B notebook, aitrends.kr/articles/94089, glossary entry "자기 조건화").
+//
+// Design (one CTA per 256 x 256 output tile and K-split):
+//   warp 0      TMA producer: A (two 128-row boxes) and B tiles of 64 K
+//               elements, 128-byte swizzle, into a 3-stage ring;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
+//               accumulators) and issues tcgen05.mma (M=128, N=256, K=16)
+//               from one thread; tcgen05.commit frees each stage;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulators (each warp reads the
+//               32 TMEM lanes of its quadrant) and fp32 stores.
+// K is split across CTAs when the tile grid alone cannot fill the 148 SMs;
+// partial tiles go to a workspace and the last CTA of a tile (atomic ticket)
+// sums them in split order, so the result does not depend on timing.
+// Every mbarrier wait is bounded (common.cuh): on timeout the CTA records
+// CANVAS_ERR_TIMEOUT, drains and returns.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace canvas {
+
+namespace {
+constexpr int kThreads = 192;
+constexpr int kABoxBytes = kGemmBM * kGemmBK * 2;          // 16 KB: 128 rows x 128 B
+constexpr int kAStageBytes = 2 * kABoxBytes;                // 32 KB
+constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;         // 32 KB
+constexpr int kTileBytes = kGemmStages * (kAStageBytes + kBStageBytes);
+constexpr int kTmemCols = 512;
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return size_t(kTileBytes) + 1024 /*align*/ + 256 /*barriers*/; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        GemmTcArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kGemmStages * kAStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTileBytes);
+  uint64_t* empty = full + kGemmStages;
+  uint64_t* tmem_full = empty + kGemmStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort, [1] last-CTA
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x, mt = blockIdx.y, split = blockIdx.z;
+  const int kb_per = g.kblocks / g.splits, kb_rem = g.kblocks % g.splits;
+  const int kb0 = split * kb_per + min(split, kb_rem);
+  const int nkb = kb_per + (split < kb_rem ? 1 : 0);
+  const int nacc = g.two_acc ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint32_t bytes = uint32_t(nacc * kABoxBytes + kBStageBytes);
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kGemmStages;
+        const uint32_t ph = (i / kGemmStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, flags)) break;
+        issued = i + 1;
+        const int kx = (kb0 + i) * kGemmBK;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* a = sA + s * kAStageBytes;
+        tma_load_2d(a, &tmA, &full[s], kx, mt * 256);
+        if (nacc == 2) tma_load_2d(a + kABoxBytes, &tmA, &full[s], kx, mt * 256 + 128);
+        uint8_t* b = sB + s * kBStageBytes;
+        if (!g.b_mn_major) {
+          tma_load_2d(b, &tmB, &full[s], kx, nt * kGemmBN);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_load_2d(b + c * 8192, &tmB, &full[s], nt * kGemmBN + 64 * c, kx);
+        }
+      }
+      // drain: every TMA this thread issued has landed before the CTA can exit
+      // (matters only after an abort; otherwise these phases are complete)
+      volatile int no_abort = 0;
+      for (int i = max(0, issued - kGemmStages); i < issued; ++i) {
+        const int s = i % kGemmStages;
+        mbar_wait(&full[s], (i / kGemmStages) & 1, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(128, 256, 0, g.b_mn_major);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kGemmStages;
+        const uint32_t ph = (i / kGemmStages) & 1;
+        if (!mbar_wait(&full[s], ph, flags)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sA + s * kAStageBytes);
+        const uint32_t b_base = smem_u32(sB + s * kBStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+          // K-major B: 16 elements = 32 bytes along the swizzled row.
+          // MN-major B: 16 K-rows = 2 groups of 8 rows x 128 B; N chunks of
+          // 64 elements sit 8 KB apart (leading byte offset).
+          const uint64_t bdesc = g.b_mn_major ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
+                                              : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+          for (int acc = 0; acc < nacc; ++acc) {
+            const uint64_t adesc = smem_desc_sw128(a_base + acc * kABoxBytes + kk * 32, 16, 1024);
+            mma_bf16_ss(tmem + acc * 256, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(tmem_full);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, quadrant = warp % 4
+    const int q = warp & 3;
+    mbar_wait(tmem_full, 0, flags);
+    tc_fence_after();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    const bool ok = flags[0] == 0;  // uniform across the epilogue warps
+    if (ok) {
+      for (int acc = 0; acc < nacc; ++acc) {
+        const int row = mt * 256 + acc * 128 + q * 32 + lane;
+        for (int cc = 0; cc < kGemmBN / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + uint32_t(acc * 256 + cc * 32) + (uint32_t(q * 32) << 16), r);
+          tmem_ld_wait();
+          const int col0 = nt * kGemmBN + cc * 32;
+          if (row >= g.M || col0 >= g.N) continue;
+          float* dst;
+          bool add;
+          if (g.splits > 1) {
+            dst = g.partials + ((size_t)split * g.M + row) * g.N + col0;
+            add = false;
+          } else {
+            dst = g.C + (size_t)row * g.ldc + col0;
+            add = g.accumulate != 0;
+          }
+          const int ncol = min(32, g.N - col0);
+          if (ncol == 32) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                     __uint_as_float(r[j + 3]));
+              float4* p = reinterpret_cast<float4*>(dst + j);
+              if (add) {
+                const float4 o = *p;
+                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+              }
+              *p = v;
+            }
+          } else {
+            for (int j = 0; j < ncol; ++j) dst[j] = (add ? dst[j] : 0.f) + __uint_as_float(r[j]);
+          }
+        }
+      }
+    }
+    if (ok && g.splits > 1) {
+      // ticket: the last CTA of this tile sums the partials in split order
+      __threadfence();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp == 2 && lane == 0) {
+        const int t = atomicAdd(&g.counters[mt * g.n_tiles + nt], 1);
+        flags[1] = (t == g.splits - 1) ? 1 : 0;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (flags[1]) {
+        __threadfence();
+        const int rows_here = nacc * 128;
+        const int col_lo = nt * kGemmBN, col_hi = min(g.N, col_lo + kGemmBN);
+        // 128 threads: each walks rows, columns in float4 steps
+        const int et = (warp - 2) * 32 + lane;
+        for (int rr = 0; rr < rows_here; ++rr) {
+          const int row = mt * 256 + rr;
+          if (row >= g.M) break;
+          for (int c = col_lo + et * 4; c < col_hi; c += 128 * 4) {
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g.accumulate) s4 = *reinterpret_cast<const float4*>(g.C + (size_t)row * g.ldc + c);
+            for (int sp = 0; sp < g.splits; ++sp) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(g.partials + ((size_t)sp * g.M + row) * g.N + c));
+              s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+            }
+            *reinterpret_cast<float4*>(g.C + (size_t)row * g.ldc + c) = s4;
+          }
+        }
+        if (warp == 2 && lane == 0) g.counters[mt * g.n_tiles + nt] = 0;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmTcArgs& g,
+                           cudaStream_t stream) {
+  static bool attr_set = false;  // per process; the attribute is per function
+  const size_t smem = gemm_tc_smem_bytes();
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(g.n_tiles, g.m_tiles, g.splits);
+  gemm_bf16_tc_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, g);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace canvas

@@ -1,0 +1,303 @@
+// sampler.cu -- the per-position vocab sampler of a denoising step.
+//
+// One thread-block cluster per canvas position (row).  Each CTA of the
+// cluster owns a contiguous slice of the vocabulary, streams it once with
+// 16-byte loads and keeps an online (max, sum, entropy-sum) state plus the
+// argmax; the CTAs swap their partial states through distributed shared
+// memory and every CTA merges them in rank order (so all agree bit for bit).
+// CTA 0 then writes the row's entropy / confidence / argmax and the
+// commit-or-renoise decision; every CTA re-reads its slice (L2-resident) and
+// writes the probabilities.
+//
+// Method: AI Trends summary of a DiffusionGemma 26B notebook
+// (aitrends.kr/articles/94089), "섹션별 상세", sampling-loop paragraph (entropy
+// per position, low-entropy positions fixed, others renoised to uniform random
+// tokens); aibars news on DiffusionGemma, "블록 자동 회귀 노이즈 제거 및 자체 수정"
+// (low-confidence tokens replaced by random tokens).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace canvas {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Online softmax state in base 2: Z = sum 2^(y - m), T = sum (y - m) 2^(y - m).
+struct RowState {
+  float m, Z, T;
+  float bx;  // best raw logit
+  int bi;    // its (lowest) index
+};
+
+__device__ __forceinline__ void state_init(RowState& s) {
+  s.m = -INFINITY;
+  s.Z = 0.f;
+  s.T = 0.f;
+  s.bx = -INFINITY;
+  s.bi = 0x7fffffff;
+}
+
+// Merge b into a (associative up to rounding; used in a fixed order).
+__device__ __forceinline__ void state_merge(RowState& a, const RowState& b) {
+  if (b.bx > a.bx || (b.bx == a.bx && b.bi < a.bi)) {
+    a.bx = b.bx;
+    a.bi = b.bi;
+  }
+  if (b.Z == 0.f) return;
+  if (a.Z == 0.f) {
+    a.m = b.m;
+    a.Z = b.Z;
+    a.T = b.T;
+    return;
+  }
+  const float M = fmaxf(a.m, b.m);
+  const float da = a.m - M, db = b.m - M;
+  const float sa = exp2f(da), sb = exp2f(db);
+  a.T = sa * (a.T + da * a.Z) + sb * (b.T + db * b.Z);
+  a.Z = sa * a.Z + sb * b.Z;
+  a.m = M;
+}
+
+// Fold a group of 8 values (already scaled to base 2 in y[]) into s.
+__device__ __forceinline__ void state_add8(RowState& s, const float (&x)[8], const float (&y)[8], int idx0) {
+  float vmax = y[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) vmax = fmaxf(vmax, y[j]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (x[j] > s.bx) {  // strict: indices increase within a thread
+      s.bx = x[j];
+      s.bi = idx0 + j;
+    }
+  }
+  if (vmax > s.m) {
+    if (s.Z != 0.f) {
+      const float dm = s.m - vmax;
+      const float sc = exp2f(dm);
+      s.T = sc * (s.T + dm * s.Z);
+      s.Z *= sc;
+    }
+    s.m = vmax;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float t = y[j] - s.m;
+    const float e = exp2f(t);
+    s.Z += e;
+    s.T = fmaf(t, e, s.T);
+  }
+}
+
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<__nv_bfloat16> {
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+};
+template <>
+struct Vec8<float> {
+  __device__ __forceinline__ static void load(const float* p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+};
+
+__device__ __forceinline__ uint64_t splitmix_out(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+}  // namespace
+
+__device__ __forceinline__ uint64_t renoise_key(uint64_t seed, uint32_t step, uint32_t row) {
+  return splitmix_out(splitmix_out(splitmix_out(seed) ^ uint64_t(step)) ^ uint64_t(row));
+}
+
+template <typename T, int kThreads>
+__global__ void __launch_bounds__(kThreads) sample_rows_kernel(SampleArgs a, const T* __restrict__ logits) {
+  constexpr int kWarps = kThreads / 32;
+  __shared__ RowState warp_part[kWarps];
+  __shared__ float cl_part[kMaxSampleCluster][5];
+  __shared__ RowState final_state;
+
+  const int row = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t csize = gridDim.x;  // cluster spans the x dimension of the grid
+  const long long c0 = (long long)rank * a.chunk;
+  const long long c1 = min((long long)a.V, c0 + a.chunk);
+  const T* lrow = logits + (long long)row * a.V;
+  const float ysc = a.inv_temp * kLog2e;
+
+  // every CTA of the cluster must be running before any DSMEM store below
+  cluster_sync_all();
+  RowState s;
+  state_init(s);
+  // pass 1: statistics
+  for (long long i = c0 + (long long)threadIdx.x * 8; i < c1; i += (long long)kThreads * 8) {
+    float x[8], y[8];
+    Vec8<T>::load(lrow + i, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = x[j] * ysc;
+    state_add8(s, x, y, int(i));
+  }
+  // warp reduce (fixed butterfly order)
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    RowState o;
+    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+    o.Z = __shfl_xor_sync(0xffffffffu, s.Z, off);
+    o.T = __shfl_xor_sync(0xffffffffu, s.T, off);
+    o.bx = __shfl_xor_sync(0xffffffffu, s.bx, off);
+    o.bi = __shfl_xor_sync(0xffffffffu, s.bi, off);
+    // lanes merge in a symmetric way so that both partners hold the same value
+    RowState lo = (threadIdx.x & off) ? o : s;
+    const RowState hi = (threadIdx.x & off) ? s : o;
+    state_merge(lo, hi);
+    s = lo;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) warp_part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RowState t = warp_part[0];
+    for (int w = 1; w < kWarps; ++w) state_merge(t, warp_part[w]);
+    // send this CTA's partial to every CTA of the cluster, slot = rank
+    const uint32_t local = smem_u32(&cl_part[rank][0]);
+    for (uint32_t dst = 0; dst < csize; ++dst) {
+      const uint32_t ra = mapa_shared(local, dst);
+      st_cluster_f32(ra + 0, t.m);
+      st_cluster_f32(ra + 4, t.Z);
+      st_cluster_f32(ra + 8, t.T);
+      st_cluster_f32(ra + 12, t.bx);
+      st_cluster_u32(ra + 16, uint32_t(t.bi));
+    }
+  }
+  cluster_sync_all();
+  if (threadIdx.x == 0) {
+    RowState t;
+    state_init(t);
+    for (uint32_t r = 0; r < csize; ++r) {
+      RowState o;
+      o.m = cl_part[r][0];
+      o.Z = cl_part[r][1];
+      o.T = cl_part[r][2];
+      o.bx = cl_part[r][3];
+      o.bi = int(__float_as_uint(cl_part[r][4]));
+      state_merge(t, o);
+    }
+    final_state = t;
+    if (rank == 0) {
+      const float H = logf(t.Z) - kLn2 * t.T / t.Z;
+      const float conf = 1.0f / t.Z;
+      a.entropy[row] = H;
+      a.confidence[row] = conf;
+      a.argmax[row] = t.bi;
+      if (a.commit_mode == 0) {
+        const bool fr = a.frozen != nullptr && a.frozen[row] != 0;
+        const bool commit = fr || (H < a.bound);
+        int tok;
+        if (fr)
+          tok = a.frozen_tokens[row];
+        else if (commit)
+          tok = t.bi;
+        else
+          tok = int(renoise_key(a.seed, a.step, uint32_t(row)) % uint64_t(a.V));
+        a.tokens[row] = tok;
+        a.commit_mask[row] = commit ? 1 : 0;
+      }
+    }
+  }
+  __syncthreads();
+  const float M = final_state.m;
+  const float invZ = 1.0f / final_state.Z;
+  // pass 2: probabilities
+  for (long long i = c0 + (long long)threadIdx.x * 8; i < c1; i += (long long)kThreads * 8) {
+    float x[8], p[8];
+    Vec8<T>::load(lrow + i, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) p[j] = exp2f(x[j] * ysc - M) * invZ;
+    const long long o = (long long)row * a.V + i;
+    if (a.probs_bf16) {
+      uint4 u;
+      u.x = pack_bf16x2(p[0], p[1]);
+      u.y = pack_bf16x2(p[2], p[3]);
+      u.z = pack_bf16x2(p[4], p[5]);
+      u.w = pack_bf16x2(p[6], p[7]);
+      *reinterpret_cast<uint4*>(a.probs_bf16 + o) = u;
+    }
+    if (a.probs_f32) {
+      float4* q = reinterpret_cast<float4*>(a.probs_f32 + o);
+      q[0] = make_float4(p[0], p[1], p[2], p[3]);
+      q[1] = make_float4(p[4], p[5], p[6], p[7]);
+    }
+  }
+}
+
+// Left-prefix commit mode: one thread per canvas walks its rows in order.
+__global__ void commit_prefix_kernel(SampleArgs a, int n_canvas) {
+  const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+  if (cv >= n_canvas) return;
+  bool run = true;
+  for (int i = 0; i < a.canvas_len; ++i) {
+    const int row = cv * a.canvas_len + i;
+    const bool fr = a.frozen != nullptr && a.frozen[row] != 0;
+    run = run && (fr || a.entropy[row] < a.bound);
+    const bool commit = fr || run;
+    int tok;
+    if (fr)
+      tok = a.frozen_tokens[row];
+    else if (commit)
+      tok = a.argmax[row];
+    else
+      tok = int(renoise_key(a.seed, a.step, uint32_t(row)) % uint64_t(a.V));
+    a.tokens[row] = tok;
+    a.commit_mask[row] = commit ? 1 : 0;
+  }
+}
+
+cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, cudaStream_t stream) {
+  constexpr int kThreads = 256;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.cluster, a.rows, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (bf16)
+    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<__nv_bfloat16, kThreads>, a,
+                           static_cast<const __nv_bfloat16*>(logits));
+  else
+    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<float, kThreads>, a, static_cast<const float*>(logits));
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  if (a.commit_mode == 1) {
+    const int n_canvas = a.rows / a.canvas_len;
+    commit_prefix_kernel<<<(n_canvas + 127) / 128, 128, 0, stream>>>(a, n_canvas);
+    e = cudaGetLastError();
+    count_launches(1);
+  }
+  return e;
+}
+
+}  // namespace canvas

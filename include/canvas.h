@@ -1,0 +1,261 @@
+/*
+ * canvas.h -- C ABI of libcanvas.so, one canvas refinement step of
+ * DiffusionGemma-style block discrete diffusion on a B300 (sm_103a).
+ *
+ * Two calls make up the step:
+ *   canvas_attention -- one fused attention layer in decode mode: QKV
+ *                       projection, scalar QK RMSNorm, split-half / partial
+ *                       RoPE, bidirectional attention of the canvas over the
+ *                       committed (paged) KV prefix plus the canvas itself.
+ *   canvas_sample    -- the per-position vocab sampler: softmax, entropy,
+ *                       argmax, confidence, entropy-bound commit / uniform
+ *                       renoise, and the self-conditioning soft embedding P.E.
+ * plus a bf16 GEMM used by callers that assemble whole layers around them.
+ *
+ * Sources (the method is described on web pages, cited by title and section):
+ *   [AIT] AI Trends summary of a DiffusionGemma 26B weights notebook
+ *         (aitrends.kr/articles/94089), "섹션별 상세" (the rms(), rotate() and
+ *         attention-block snippets; the sampling-loop paragraph) and the
+ *         glossary "용어 해설".
+ *   [TC]  ThakiCloud, "DiffusionGemma 26B-A4B", "아키텍처".
+ *   [AB]  aibars news on DiffusionGemma, "블록 자동 회귀 노이즈 제거 및 자체 수정".
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is DEVICE memory unless its comment says "host".
+ *     The caller owns all memory; no call allocates device memory.
+ *   - Calls are asynchronous: they validate arguments on the host, enqueue
+ *     kernels on `stream` and return.  They never synchronise.  Errors found
+ *     on the device (a cache page index out of range, a bounded wait that ran
+ *     out) are recorded in a per-device status word that
+ *     canvas_device_status() reads.
+ *   - A status other than CANVAS_OK leaves a message for
+ *     canvas_last_error() (thread-local).  Shapes the kernels do not cover
+ *     return CANVAS_ERR_UNSUPPORTED; there is no fallback path.
+ *   - Calls on different streams may run concurrently if they use distinct
+ *     workspaces.  Calls that share a workspace must be stream-ordered.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef CANVAS_H_
+#define CANVAS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* canvas_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  CANVAS_OK = 0,
+  CANVAS_ERR_ARG = -1,          /* bad pointer, size, or combination of flags */
+  CANVAS_ERR_UNSUPPORTED = -2,  /* valid request outside what the kernels cover */
+  CANVAS_ERR_CUDA = -3,         /* a CUDA runtime / driver call failed */
+  CANVAS_ERR_TIMEOUT = -4,      /* a bounded device-side wait ran out */
+  CANVAS_ERR_WORKSPACE = -5,    /* workspace NULL, too small or misaligned */
+  CANVAS_ERR_BOUNDS = -6        /* device-side index check failed (e.g. a page id) */
+} canvas_status;
+
+typedef enum { CANVAS_BF16 = 0, CANVAS_FP32 = 1 } canvas_dtype;
+
+typedef enum {
+  /* local layer: the cache holds final keys (normed, rotated) and values;
+     prefix tokens more than `window` positions back are not visible */
+  CANVAS_LAYER_SLIDING = 0,
+  /* global (full-attention) layer: W_v = W_k, the cache holds the raw shared
+     projection r; key = rotate(rms(r)) at the key's position, value = r */
+  CANVAS_LAYER_GLOBAL = 1
+} canvas_layer_type;
+
+/*
+ * Paged KV cache of the committed prefix.  Caller-owned device memory.
+ *
+ * k_pool  [num_pages][Hkv][page_tokens][d], element type = the call's dtype.
+ *         Sliding layers: final keys.  Global layers: raw shared rows r.
+ * v_pool  same layout: values (sliding layers); must be NULL on global layers.
+ * block_table [B][max_pages_per_seq] int32: physical page of logical page p
+ *         of sequence b (tokens p*page_tokens ...).  Entries for pages that hold
+ *         no visible token may be -1; entries that are read must lie in
+ *         [0, num_pages), else the call records CANVAS_ERR_BOUNDS.
+ * page_tokens must be a multiple of 64 for bf16 calls (of 16 for fp32 calls).
+ */
+typedef struct {
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_table;
+  int32_t max_pages_per_seq;
+  int32_t page_tokens;
+  int32_t num_pages;
+} canvas_kv_cache;
+
+/*
+ * Workspace (bytes) that canvas_attention needs for this shape.  The same
+ * arguments must be passed to the call.  Returns 0 for an invalid shape.
+ */
+size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, int Hkv, int d,
+                                       int max_prefix, int layer_type);
+
+/*
+ * canvas_attention -- one attention layer of a canvas refinement step.
+ *
+ * Defined by [AIT] "섹션별 상세": the attention-block snippet (projection,
+ * 'l (n h) -> n l h', rms() on q and k, rotate() on q and k, then cache
+ * concatenation and attention), the rms() snippet (w * x * sqrt(d) /
+ * (||x||_2 + eps), norm in fp32), the rotate() snippet (split-half pairs
+ * t, t+d/2; angle (l + start) * freq[t mod d/2]) and the decode-mode paragraph
+ * (the canvas attends bidirectionally to committed past | current canvas;
+ * W_v = W_k on full-attention layers, where only K is normed and rotated);
+ * the glossary entries on partial RoPE and sliding-window attention; window
+ * 1,024 per [TC] "아키텍처".
+ *
+ *   x        [B, C, D]            canvas input, dtype (row-major)
+ *   W_q      [Hq*d, D]            dtype;  q = x W_q^T
+ *   W_k      [Hkv*d, D]           dtype;  k = x W_k^T
+ *   W_v      [Hkv*d, D] or NULL   dtype;  NULL only on global layers (W_v = W_k)
+ *   gamma_q, gamma_k [d] fp32     QK-norm weights.  On global layers gamma_k
+ *                                 must be constant-valued (the pages report
+ *                                 constant learned vectors); a kernel checks
+ *                                 it and records CANVAS_ERR_UNSUPPORTED.
+ *   eps                           rms epsilon, added to ||x||_2
+ *   freq     [d/2] fp32           RoPE spectrum; zero entries are not rotated
+ *   layer_type                    canvas_layer_type
+ *   kv       host pointer to the cache descriptor (device pointers inside)
+ *   prefix_len [B] int32          committed prefix length of each sequence;
+ *                                 canvas position i sits at prefix_len[b] + i
+ *   max_prefix                    host: upper bound of prefix_len[] (sizes grids
+ *                                 and the workspace); a larger prefix_len[b]
+ *                                 records CANVAS_ERR_BOUNDS
+ *   window                        sliding layers: a canvas row at position p
+ *                                 sees prefix keys j >= p - window; <= 0 means
+ *                                 the whole prefix.  Ignored on global layers.
+ *   scale                         multiplies q.k (1.0: the QK norm already
+ *                                 fixes the temperature)
+ *   v_unit_rms                    0 (default).  1 on a global layer: value =
+ *                                 sqrt(d) * r / (||r|| + eps)
+ *   out      [B, C, Hq*d] dtype   heads concatenated, 'n l h -> l (n h)'
+ *   lse      [B, C, Hq] fp32 or NULL   natural-log softmax normaliser
+ *   workspace, ws_bytes           >= canvas_attention_workspace_size(...),
+ *                                 256-byte aligned; contents are scratch
+ *
+ * Supported: dtype BF16 with d in {64, 128, 256, 512}, D % 8 == 0; dtype FP32
+ * with d <= 512.  Hq % Hkv == 0, d even, C >= 1.
+ */
+canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D,
+                               const void* W_q, const void* W_k, const void* W_v,
+                               int Hq, int Hkv, int d,
+                               const float* gamma_q, const float* gamma_k, float eps,
+                               const float* freq, int layer_type,
+                               const canvas_kv_cache* kv,
+                               const int32_t* prefix_len, int max_prefix, int window,
+                               float scale, int v_unit_rms,
+                               void* out, float* lse,
+                               void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
+/* Workspace (bytes) that canvas_sample needs; 0 for an invalid shape. */
+size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
+
+/*
+ * canvas_sample -- the sampler of one denoising step, per canvas position.
+ *
+ * Defined by [AIT] "섹션별 상세", the sampling-loop paragraph (per-position
+ * entropy; positions within the entropy bound are fixed, the rest renoised to
+ * uniformly random tokens), [AB] "블록 자동 회귀 노이즈 제거 및 자체 수정"
+ * (low-confidence tokens swapped for random tokens), and the self-conditioning
+ * glossary entry of [AIT] (expected embedding P.E of the softmax).
+ *
+ *   logits   [rows, V] dtype      rows = B*C positions
+ *   E        [V, D] dtype         embedding table (row-major)
+ *   entropy_bound                 commit iff entropy < bound (nats, strict)
+ *   seed, step                    renoise key = m(m(m(seed) ^ step) ^ row),
+ *                                 m = one SplitMix64 output; token = key mod V
+ *   temperature                   logits are divided by it (> 0)
+ *   commit_mode                   0: per position; 1: the longest run of
+ *                                 qualifying positions from the left of each
+ *                                 canvas of canvas_len rows
+ *   canvas_len                    C (rows % C == 0 in mode 1)
+ *   frozen   [rows] uint8 or NULL       1: position already committed; it keeps
+ *   frozen_tokens [rows] int32 or NULL  its token and counts as committed
+ *   tokens   [rows] int32         out: frozen token / argmax / renoise token
+ *   commit_mask [rows] uint8      out: 1 = committed
+ *   entropy, confidence [rows] fp32  out: -sum p ln p, max p
+ *   argmax   [rows] int32 or NULL out: lowest index of the largest logit
+ *   probs_out [rows, V] or NULL   out: softmax, in probs_dtype
+ *   probs_dtype                   CANVAS_BF16 or CANVAS_FP32
+ *   soft_emb [rows, D] fp32       out: P.E.  bf16 calls multiply the bf16
+ *                                 probabilities; fp32 calls the fp32 ones.
+ *   workspace, ws_bytes           >= canvas_sample_workspace_size(...)
+ *
+ * Supported: V % 8 == 0, D % 8 == 0, rows >= 1.
+ */
+canvas_status canvas_sample(const void* logits, int dtype, int rows, int V,
+                            const void* E, int D, float entropy_bound,
+                            uint64_t seed, uint32_t step, float temperature,
+                            int commit_mode, int canvas_len,
+                            const uint8_t* frozen, const int32_t* frozen_tokens,
+                            int32_t* tokens, uint8_t* commit_mask, float* entropy,
+                            float* confidence, int32_t* argmax,
+                            void* probs_out, int probs_dtype, float* soft_emb,
+                            void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
+/* Workspace (bytes) that canvas_gemm_bf16 needs for this shape. */
+size_t canvas_gemm_workspace_size(int M, int N, int K);
+
+/*
+ * canvas_gemm_bf16 -- C[M,N] (fp32) = A[M,K] . op(B)  (+ C if accumulate).
+ *
+ * Glue for callers that build whole layers (output projection, tied LM head)
+ * and the soft-embedding product; the pages write these as plain matrix
+ * products ([AIT] "섹션별 상세": x @ W.T).
+ *   A  [M, K] bf16 row-major (K contiguous)
+ *   B  b_layout 0: [N, K] row-major ("weights", C = A B^T)
+ *      b_layout 1: [K, N] row-major (C = A B)
+ *   C  [M, N] fp32 row-major, leading dimension N
+ * Requires K % 8 == 0 and N % 8 == 0 (16-byte aligned rows).
+ */
+canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float* C,
+                               int M, int N, int K, int accumulate,
+                               void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
+/*
+ * Kernel timing hooks, for benchmarks.  When a pair of events is registered
+ * for a kernel id, every later call on this thread records `start` on the
+ * call's stream immediately before that kernel's launch and `stop` right
+ * after it, so cudaEventElapsedTime gives the kernel's device time.  Events
+ * are cudaEvent_t handles owned by the caller; pass NULL, NULL to clear.
+ *   CANVAS_KERNEL_ATTENTION  -- the attention core of canvas_attention
+ *   CANVAS_KERNEL_PREP       -- everything canvas_attention runs before it
+ *                               (QKV projection, QK norm + RoPE, key prep)
+ *   CANVAS_KERNEL_SAMPLER    -- the vocab reduction of canvas_sample
+ *   CANVAS_KERNEL_SOFT_EMB   -- the soft-embedding GEMM of canvas_sample
+ */
+typedef enum {
+  CANVAS_KERNEL_ATTENTION = 0,
+  CANVAS_KERNEL_PREP = 1,
+  CANVAS_KERNEL_SAMPLER = 2,
+  CANVAS_KERNEL_SOFT_EMB = 3,
+  CANVAS_KERNEL_COUNT = 4
+} canvas_kernel_id;
+canvas_status canvas_profile_events(int kernel_id, void* start_event, void* stop_event);
+
+/* Number of kernels this library has launched in this process (host count). */
+uint64_t canvas_kernel_launches(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* canvas_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: CANVAS_OK, or the first error a kernel recorded since the
+ * last read (CANVAS_ERR_BOUNDS, CANVAS_ERR_TIMEOUT, CANVAS_ERR_UNSUPPORTED).
+ * This is the only call that synchronises.
+ */
+canvas_status canvas_device_status(canvas_stream_t stream);
+
+/* Library version string. */
+const char* canvas_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CANVAS_H_ */

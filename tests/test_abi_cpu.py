@@ -1,0 +1,64 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments on the host
+(before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import canvas_denoising_step_03_b300 as cv
+    return cv
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "canvas.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(canvas_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(cv):
+    syms = header_symbols()
+    assert "canvas_attention" in syms and "canvas_sample" in syms
+    for s in syms:
+        assert hasattr(cv.lib, s), s
+    assert sorted(cv.EXPORTED) == syms
+    assert cv.canvas_version().startswith("canvas")
+
+
+def test_workspace_sizes_are_positive_and_reject_bad_shapes(cv):
+    assert cv.canvas_attention_workspace_size(cv.CANVAS_BF16, 1, 256, 2816, 16, 2, 512, 32768, 1) > 0
+    assert cv.canvas_attention_workspace_size(cv.CANVAS_BF16, 1, 256, 2816, 16, 3, 512, 32768, 1) == 0
+    assert cv.canvas_sample_workspace_size(cv.CANVAS_BF16, 256, 262144, 2816) > 256 * 262144 * 2
+    assert cv.canvas_gemm_workspace_size(256, 2816, 262144) > 0
+    assert cv.canvas_gemm_workspace_size(0, 1, 1) == 0
+
+
+def test_host_validation_errors(cv):
+    lib = cv.lib
+    kv = cv.canvas_kv_cache()
+    # null pointers -> CANVAS_ERR_ARG, message set, no CUDA work
+    st = lib.canvas_attention(None, cv.CANVAS_BF16, 1, 16, 128, None, None, None, 2, 1, 64, None, None, 1e-6,
+                              None, 0, ctypes.byref(kv), None, 0, 0, 1.0, 0, None, None, None, 0, None)
+    assert st == cv.CANVAS_ERR_ARG
+    assert "null" in cv.canvas_last_error()
+    st = lib.canvas_sample(None, cv.CANVAS_BF16, 4, 512, None, 64, 0.3, 0, 0, 1.0, 0, 4, None, None, None, None,
+                           None, None, None, None, 0, None, None, 0, None)
+    assert st == cv.CANVAS_ERR_ARG
+    st = lib.canvas_gemm_bf16(None, None, 0, None, 4, 8, 8, 0, None, 0, None)
+    assert st == cv.CANVAS_ERR_ARG
+    # unsupported K alignment, checked before the workspace
+    fake = ctypes.c_void_p(256)
+    st = lib.canvas_gemm_bf16(fake, fake, 0, fake, 4, 8, 12, 0, fake, 1 << 20, None)
+    assert st == cv.CANVAS_ERR_UNSUPPORTED
+    # workspace too small
+    st = lib.canvas_gemm_bf16(fake, fake, 0, fake, 4, 8, 16, 0, fake, 16, None)
+    assert st == cv.CANVAS_ERR_WORKSPACE

@@ -1,0 +1,109 @@
+"""canvas_attention through the C ABI against the fp64 oracle.
+
+Tolerances: bf16 calls -- max |err| <= 2e-2 and relative Frobenius error
+<= 5e-3 (the bar set for the attention output in bf16); fp32 calls -- 1e-4 /
+1e-5 (fp32 arithmetic against fp64).
+"""
+import numpy as np
+import pytest
+import torch
+
+import canvas_workloads as wl
+from canvas_harness import AttnCase, attn_errors, oracle_attention
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_FRO = 2e-2, 5e-3
+FP32_MAX, FP32_FRO = 1e-4, 1e-5
+
+
+@pytest.fixture(scope="module")
+def cv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import canvas_denoising_step_03_b300 as cv
+    return cv
+
+
+def small(**kw):
+    base = dict(name="small", B=2, C=80, prefix=(300, 130), D=256, Hq=4, Hkv=2, d=128, layer="sliding",
+                window=96, theta=1e4, rotary_fraction=1.0, dtype="bf16", seed=21, page_tokens=64)
+    base.update(kw)
+    return wl.AttnConfig(**base)
+
+
+def check(cv, cfg, rows=None, v_unit_rms=False, page_seed=1234):
+    inp = wl.make_attention_inputs(cfg)
+    case = AttnCase(inp, page_seed=page_seed).run(v_unit_rms=int(v_unit_rms))
+    assert case.status() == cv.CANVAS_OK, cv.canvas_last_error()
+    want, want_lse = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms)
+    got = case.out_f64()
+    mx, rf = attn_errors(got, want)
+    lse = case.lse.cpu().numpy().astype(np.float64)
+    m = np.isfinite(want_lse)
+    lse_err = float(np.max(np.abs(lse[m] - want_lse[m]) / (1.0 + np.abs(want_lse[m]))))
+    if cfg.dtype == "bf16":
+        assert mx <= BF16_MAX and rf <= BF16_FRO, (mx, rf)
+    else:
+        assert mx <= FP32_MAX and rf <= FP32_FRO, (mx, rf)
+    assert lse_err < 1e-3, lse_err
+    if rows is None:
+        assert np.all(np.isfinite(got))
+    return mx, rf
+
+
+def test_tiny_fp32_workload(cv):
+    check(cv, wl.TINY)
+
+
+@pytest.mark.parametrize("cfg", [
+    small(),                                                   # sliding, ragged prefix, window inside prefix
+    small(window=0),                                           # sliding, whole prefix visible
+    small(window=1000),                                        # window longer than the prefix
+    small(prefix=(0, 64), C=33),                               # empty prefix / page-aligned prefix
+    small(B=1, C=1, prefix=(70,), Hq=2, Hkv=1),                # one canvas token
+    small(Hq=8, Hkv=1, d=256, D=512),                          # GQA 8:1, head_dim 256
+    small(layer="global", window=0, theta=1e6, rotary_fraction=0.25),
+    small(layer="global", window=0, theta=1e6, rotary_fraction=0.25, Hq=8, Hkv=1, d=512, D=512,
+          prefix=(200, 64), C=64),
+    small(dtype="fp32", page_tokens=16),
+    small(dtype="fp32", layer="global", window=0, theta=1e6, rotary_fraction=0.25, page_tokens=32),
+], ids=lambda c: f"{c.layer}-{c.dtype}-B{c.B}C{c.C}P{'_'.join(map(str, c.prefix))}-H{c.Hq}x{c.Hkv}d{c.d}w{c.window}")
+def test_small_shapes(cv, cfg):
+    check(cv, cfg)
+
+
+def test_global_unit_rms_value_variant(cv):
+    check(cv, small(layer="global", window=0, theta=1e6, rotary_fraction=0.25), v_unit_rms=True)
+
+
+def test_page_permutation_does_not_change_the_result(cv):
+    cfg = small()
+    inp = wl.make_attention_inputs(cfg)
+    a = AttnCase(inp, page_seed=1).run()
+    b = AttnCase(inp, page_seed=2).run()
+    assert cv.canvas_device_status() == cv.CANVAS_OK
+    assert not np.array_equal(a.table_np, b.table_np)
+    assert torch.equal(a.out, b.out)
+
+
+def test_bad_page_id_reports_bounds_error(cv):
+    cfg = small()
+    inp = wl.make_attention_inputs(cfg)
+    case = AttnCase(inp)
+    case.block_table[0, 4] = 10_000          # a visible page of sequence 0 outside the pool: checked, not read
+    case.run()
+    assert case.status() == cv.CANVAS_ERR_BOUNDS
+    assert cv.canvas_device_status() == cv.CANVAS_OK  # the word was cleared
+
+
+def test_sliding_layer_workload(cv):
+    """Sliding-window layer: batch 1, canvas 256, prefix 4096, 16/8 heads, head_dim 256, window 1024 (all rows)."""
+    check(cv, wl.SLIDING)
+
+
+def test_global_layer_workload_sampled_rows(cv):
+    """Global layer: batch 1, canvas 256, prefix 32768, 16/2 heads, head_dim 512 -- every head at a spread of
+    canvas rows (the oracle scores all 33024 keys of each)."""
+    rows = [(0, h, i) for h in range(16) for i in (0, 1, 77, 128, 200, 255)]
+    check(cv, wl.GLOBAL, rows=rows)
