@@ -33,23 +33,35 @@ Readings where the pages are silent (each is listed in the design notes):
 
 Storage model (``storage='bf16'``).  The path keeps some tensors in bf16
 memory; there the value is rounded to bf16 once, at the point it is stored,
-and every other step is exact fp64.  The rounded tensors are:
+and every other step is exact fp64.  The page's rms() and rotate() snippets
+cast their results back to the input dtype, so a normed, rotated row is a
+stored row.  The rounded tensors are:
 
-* the canvas query after norm and rotation (the page's rotate() casts its
-  result to the input dtype);
-* on sliding layers the canvas key after norm and rotation, and the canvas
-  value;
-* on global layers the canvas's raw shared projection r (it becomes part of
-  the key set exactly like a cached row) and, for every key row, the rotation
-  rotate(r) of the raw row.  Because rms multiplies a row by the scalar
-  sqrt(d) / (||r|| + eps) and the per-layer QK-norm vector is constant
-  ([AIT] glossary, scalar QK norm), rotate(rms(r, gamma_k)) equals
-  gamma_k * sqrt(d) / (||r|| + eps) * rotate(r); the path stores rotate(r) in
-  bf16 and applies the scalar to the score.  This mode requires a constant
-  gamma_k on global layers.
+* the canvas query after norm and rotation;
+* the canvas projections that become key / value rows: on sliding layers the
+  canvas key after norm and rotation and the canvas value x W_v^T; on global
+  layers the canvas's raw shared projection r = x W_k^T (it joins the key set
+  exactly like a cached row);
+* on global layers the key of every row, rotate(rms(r, gamma_k)) at the row's
+  own position.  The unit-RMS value variant keeps the stored row r and its
+  exact row scalar (no further rounding).
 
 ``storage='fp64'`` applies no rounding anywhere (the pages' formulas as
 written, evaluated exactly).
+
+Rounding slack.  A stored bf16 value is a decision taken in floating point:
+when the exact value lies within the path's own arithmetic error of a bf16
+rounding midpoint, both neighbours are correct stored values, and attention
+with its sharp softmax can turn one such flip into a visible change of the
+output.  With ``slack_eps`` set, the oracle also returns, per output element,
+a bound on how far the output can move under every combination of such
+flips: an element x is ambiguous when |x - midpoint| <= slack_eps * (|x| +
+|partner| + rms(row)) (partner: the other element of its rotation pair), and
+the bound propagates the one-ulp alternatives exactly through the softmax:
+with logit moves |delta_j| <= D_j and Zmax = sum_j p_j exp(D_j), every
+probability ratio p'_j / p_j lies within [exp(-D_j) / Zmax, Zmax exp(D_j)],
+so |o' - o| <= sum_j p_j (Zmax e^{D_j} - 1) |v_j - o| + sum_j p_j Zmax e^{D_j}
+|dv_j|.
 """
 from __future__ import annotations
 
@@ -60,20 +72,69 @@ import numpy as np
 from .numerics import bf16_round, rms, rotate
 
 
-def _maybe_round(a, storage):
-    return bf16_round(a) if storage == "bf16" else a
+def _step(r: np.ndarray, direction: int) -> np.ndarray:
+    """The next bf16 value from bf16 value r towards +inf (1) or -inf (-1)."""
+    r = np.asarray(r, np.float64)
+    out = np.empty_like(r)
+    bits = _bf16_bits(r)
+    # bf16 values are ordered like sign-magnitude integers
+    pos = r > 0
+    neg = r < 0
+    zero = r == 0
+    up = direction > 0
+    nb = np.where(pos, bits + (1 if up else -1), np.where(neg, bits - (1 if up else -1), 0))
+    out = _from_bits(nb)
+    if zero.any():
+        tiny = np.ldexp(1.0, -133)      # smallest positive bf16 subnormal
+        out = np.where(zero, tiny if up else -tiny, out)
+    return out
 
 
-def _global_keys(r: np.ndarray, pos0: int, gamma_k: np.ndarray, freq, eps: float, storage: str):
-    """Keys of raw shared rows r [L, d] sitting at positions pos0 .. pos0+L-1."""
-    d = r.shape[-1]
-    if storage == "bf16":
-        g = np.asarray(gamma_k, np.float64)
-        if not np.all(g == g[0]):
-            raise ValueError("bf16 storage model on global layers needs a constant gamma_k")
-        s = np.sqrt(d) / (np.sqrt(np.sum(r * r, axis=-1, keepdims=True)) + eps)
-        return g[0] * s * bf16_round(rotate(r, freq, pos0))
-    return rotate(rms(r, gamma_k, eps), freq, pos0)
+def _bf16_bits(r):
+    f = np.asarray(r, np.float64).astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.int64)
+
+
+def _from_bits(b):
+    u = (np.asarray(b, np.int64).astype(np.uint32) << np.uint32(16))
+    return u.view(np.float32).astype(np.float64)
+
+
+def rounding_flips(x: np.ndarray, partner: np.ndarray, eps: float):
+    """Stored bf16 value of x and the signed change to the other neighbour
+    where the rounding is ambiguous (0 elsewhere).
+
+    Ambiguous: |x - midpoint(lo, hi)| <= eps * (|x| + |partner| + rms of the
+    row), i.e. within the arithmetic error a path that computes x in fp32
+    makes before rounding.
+    """
+    x = np.asarray(x, np.float64)
+    stored = bf16_round(x)
+    lo = np.where(stored > x, _step(stored, -1), stored)
+    hi = np.where(stored > x, stored, _step(stored, +1))
+    exact = (stored == x)
+    mid = 0.5 * (lo + hi)
+    row_rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
+    tol = eps * (np.abs(x) + np.abs(partner) + row_rms)
+    amb = (np.abs(x - mid) <= tol) & ~exact
+    alt = np.where(stored == lo, hi, lo)
+    delta = np.where(amb, alt - stored, 0.0)
+    return stored, delta
+
+
+def _pair_partner(x: np.ndarray) -> np.ndarray:
+    """The other element of each split-half rotation pair (t <-> t + d/2)."""
+    h = x.shape[-1] // 2
+    return np.concatenate([x[..., h:], x[..., :h]], axis=-1)
+
+
+def _store(x, storage, slack_eps, partner=None):
+    """(stored value, flip delta or None) of a tensor the path keeps in bf16."""
+    if storage != "bf16":
+        return x, None
+    if slack_eps is None:
+        return bf16_round(x), None
+    return rounding_flips(x, _pair_partner(x) if partner is None else partner, slack_eps)
 
 
 def visible_prefix(P: int, i: int, window: int, layer: str) -> range:
@@ -83,10 +144,24 @@ def visible_prefix(P: int, i: int, window: int, layer: str) -> range:
     return range(max(0, P + i - window), P)
 
 
+def _row_slack(q, dq, keys, dkeys, vals, dvals, p, o, scale):
+    """Bound on |o' - o| for one query row under every combination of flips.
+
+    q, dq [d]; keys, dkeys, vals, dvals [n, d]; p [n] softmax weights; o [d].
+    Logit move bound D_j = scale * (|dq| . (|k_j| + |dk_j|) + |q| . |dk_j|).
+    """
+    aq, adq = np.abs(q), np.abs(dq)
+    D = abs(scale) * ((np.abs(keys) + np.abs(dkeys)) @ adq + np.abs(dkeys) @ aq)
+    ed = np.exp(D)
+    zmax = float(p @ ed)
+    w = p * (zmax * ed - 1.0)
+    return w @ np.abs(vals - o) + (p * zmax * ed) @ np.abs(dvals)
+
+
 def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma_k,
                      eps: float, freq, layer: str, cache_k, cache_v, prefix_len, window: int,
                      scale: float = 1.0, v_unit_rms: bool = False, storage: str = "fp64",
-                     rows: Optional[Iterable] = None):
+                     rows: Optional[Iterable] = None, slack_eps: Optional[float] = None):
     """Decode-mode canvas attention for one layer.
 
     Arguments are exact fp64 values (the stored inputs widened).  Shapes:
@@ -96,7 +171,9 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
 
     Returns (out [B, C, Hq*d], lse [B, C, Hq]); lse is the natural-log
     normaliser of each softmax row.  ``rows`` optionally restricts the work to
-    a list of (b, h, i) triples; the other entries are NaN.
+    a list of (b, h, i) triples; the other entries are NaN.  With
+    ``slack_eps`` (bf16 storage only) a third array [B, C, Hq*d] holds the
+    rounding slack of every output element (module docstring).
     """
     x = np.asarray(x, np.float64)
     B, C, D = x.shape
@@ -108,6 +185,7 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
         raise ValueError("global layers share W_v = W_k")
     if v_unit_rms and layer != "global":
         raise ValueError("v_unit_rms applies to global layers only")
+    want_slack = slack_eps is not None and storage == "bf16"
 
     # 1-2: projections and head split: [B, H, C, d]
     def heads(z, H):
@@ -119,30 +197,50 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
 
     out = np.full((B, C, Hq * d), np.nan)
     lse = np.full((B, C, Hq), np.nan)
+    slack = np.full((B, C, Hq * d), np.nan) if want_slack else None
     wanted = None if rows is None else {(int(b), int(h), int(i)) for (b, h, i) in rows}
+    sl_eps = slack_eps if want_slack else None
+
+    def zeros_like(a):
+        return np.zeros_like(a)
 
     for b in range(B):
         P = int(prefix_len[b])
         # 3-4: queries of this sequence, [Hq, C, d]
-        q = rotate(rms(q_raw[b], gamma_q, eps), freq, P)
-        q = _maybe_round(q, storage)
+        q, dq = _store(rotate(rms(q_raw[b], gamma_q, eps), freq, P), storage, sl_eps)
         for hk in range(Hkv):
             # the key / value rows of this KV head: prefix then canvas
             if layer == "sliding":
                 kp = np.asarray(cache_k[b, hk, :P], np.float64)
                 vp = np.asarray(cache_v[b, hk, :P], np.float64)
-                kc = _maybe_round(rotate(rms(k_raw[b, hk], gamma_k, eps), freq, P), storage)
-                vc = _maybe_round(v_raw[b, hk], storage)
+                kc, dkc = _store(rotate(rms(k_raw[b, hk], gamma_k, eps), freq, P), storage, sl_eps)
+                vc, dvc = _store(v_raw[b, hk], storage, sl_eps)
+                dkp, dvp = zeros_like(kp), zeros_like(vp)
             else:
                 rp = np.asarray(cache_k[b, hk, :P], np.float64)
-                rc = _maybe_round(k_raw[b, hk], storage)
-                kp = _global_keys(rp, 0, gamma_k, freq, eps, storage)
-                kc = _global_keys(rc, P, gamma_k, freq, eps, storage)
+                rc, drc = _store(k_raw[b, hk], storage, sl_eps)
+                r = np.concatenate([rp, rc], axis=0)
+                kk, dkk = _store(rotate(rms(r, gamma_k, eps), freq, 0), storage, sl_eps)
+                kp, kc = kk[:P], kk[P:]
                 if v_unit_rms:
-                    vp = np.sqrt(d) * rp / (np.sqrt(np.sum(rp * rp, -1, keepdims=True)) + eps)
-                    vc = np.sqrt(d) * rc / (np.sqrt(np.sum(rc * rc, -1, keepdims=True)) + eps)
+                    # the row scalar sqrt(d) / (|r| + eps) is applied in fp32 to
+                    # the softmax weight of the row; the value row stays r
+                    vv = np.sqrt(d) * r / (np.sqrt(np.sum(r * r, -1, keepdims=True)) + eps)
                 else:
-                    vp, vc = rp, rc
+                    vv = r
+                vp, vc = vv[:P], vv[P:]
+                if want_slack:
+                    # a flip of a canvas r element moves that row's key (through
+                    # rms and rotate: at most |gamma_k| s (|dr_t| + |dr_pair|))
+                    # and its value (dr itself, or its unit-RMS image)
+                    nr = np.sqrt(np.sum(rc * rc, -1, keepdims=True))
+                    s_row = np.sqrt(d) / (nr + eps)
+                    prop = np.max(np.abs(gamma_k)) * s_row * (np.abs(drc) + np.abs(_pair_partner(drc)))
+                    dkk = np.abs(dkk)
+                    dkk[P:] += prop * 1.01
+                    dvv = np.concatenate([np.zeros_like(rp), np.abs(drc) * (s_row * 1.01 if v_unit_rms else 1.0)])
+                    dkp, dkc = dkk[:P], dkk[P:]
+                    dvp, dvc = dvv[:P], dvv[P:]
             for g in range(G):
                 h = hk * G + g
                 for i in range(C):
@@ -155,8 +253,16 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     m = np.max(s)
                     e = np.exp(s - m)
                     Z = np.sum(e)
-                    out[b, i, h * d:(h + 1) * d] = (e / Z) @ vals
+                    o = (e / Z) @ vals
+                    out[b, i, h * d:(h + 1) * d] = o
                     lse[b, i, h] = m + np.log(Z)
+                    if want_slack:
+                        dkeys = np.concatenate([dkp[vis.start:vis.stop], dkc], axis=0)
+                        dvals = np.concatenate([dvp[vis.start:vis.stop], dvc], axis=0)
+                        slack[b, i, h * d:(h + 1) * d] = _row_slack(q[h, i], dq[h, i], keys, dkeys, vals, dvals,
+                                                                    e / Z, o, scale)
+    if want_slack:
+        return out, lse, slack
     return out, lse
 
 

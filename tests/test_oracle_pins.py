@@ -367,3 +367,94 @@ def test_renoise_key_composition():
     s2 = osm.stream(s1 ^ 129, 1)[0]
     assert osm.renoise_key(7, 3, 129) == s2
     assert osm.renoise_token(7, 3, 129, 262144) == s2 & (262144 - 1)
+
+
+# ---------------------------------------------------------------- bf16 rounding slack
+def test_rounding_flips_hand_cases():
+    # 1 + 2^-8 + tiny lies just above the midpoint of 1 and 1 + 2^-7: it rounds
+    # up, and the other neighbour 1 is one ulp below
+    x = np.array([[1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -9, 1.5, -1.0 - 2.0 ** -8 - 2.0 ** -20]])
+    partner = np.zeros_like(x)
+    stored, delta = oatt.rounding_flips(x, partner, 2.0 ** -16)
+    np.testing.assert_array_equal(stored, onum.bf16_round(x))
+    assert stored[0, 0] == 1.0 + 2.0 ** -7 and delta[0, 0] == -(2.0 ** -7)
+    assert delta[0, 1] == 0.0          # a quarter ulp from the nearest value: far from any midpoint
+    assert delta[0, 2] == 0.0          # exactly representable
+    assert stored[0, 3] == -1.0 - 2.0 ** -7 and delta[0, 3] == 2.0 ** -7
+    # a window too small to reach the midpoint flags nothing
+    _, d0 = oatt.rounding_flips(x, partner, 2.0 ** -30)
+    assert not d0.any()
+
+
+@pytest.mark.parametrize("layer", ["sliding", "global"])
+def test_rounding_slack_bounds_every_flip_combination(layer):
+    # Nudging the inputs by a relative 1e-5 moves every pre-rounding value far
+    # less than the ambiguity window (2^-12 of the row scale), so each perturbed
+    # run flips some subset of the flagged roundings and nothing else: its
+    # output must stay within the slack of the nominal run (plus the ~1e-5
+    # continuous change of the nudge).
+    cfg = _small_cfg(B=1, C=24, prefix=(90,), D=48, Hq=4, Hkv=2, d=32, window=40, dtype="bf16", gamma_q=2.0,
+                     gamma_k=2.0, seed=13, layer=layer, theta=1e4 if layer == "sliding" else 1e6,
+                     rotary_fraction=1.0 if layer == "sliding" else 0.25)
+    inp = wl.make_attention_inputs(cfg)
+    ref, _, slack = _run_oracle(inp, "bf16", slack_eps=2.0 ** -12)
+    assert np.all(slack >= 0) and slack.max() > 0
+    rng = np.random.default_rng(0)
+    moved = 0.0
+    for _ in range(6):
+        x = _f64(inp, "x") * (1.0 + 1e-5 * rng.standard_normal(_f64(inp, "x").shape))
+        c = inp.cfg
+        alt, _ = oatt.canvas_attention(x, _f64(inp, "W_q"), _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hq, c.Hkv, c.d,
+                                       inp.gamma_q, inp.gamma_k, c.eps, inp.freq, c.layer, _f64(inp, "cache_k"),
+                                       _f64(inp, "cache_v"), inp.prefix_len, c.window, storage="bf16")
+        d = np.abs(alt - ref)
+        assert np.all(d <= slack + 1e-4), float(np.max(d - slack))
+        moved = max(moved, float(d.max()))
+    assert moved > 1e-3   # some ambiguous rounding did flip: the check is not vacuous
+
+
+def test_rounding_slack_is_zero_without_bf16_storage():
+    cfg = _small_cfg()
+    inp = wl.make_attention_inputs(cfg)
+    out = _run_oracle(inp, "fp64", slack_eps=2.0 ** -14)
+    assert len(out) == 2   # fp64 storage has no rounding decisions to bound
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v"])
+def test_row_slack_bounds_brute_force_flips(which):
+    # One query row, 5 keys, d = 4; ambiguous elements only in q, only in the
+    # keys, or only in the values.  Enumerate every combination of flips and
+    # evaluate the softmax output exactly: the largest change must stay within
+    # the bound, and the bound must not be vacuous (it moves when flips do).
+    rng = np.random.default_rng(7)
+    d, n = 4, 5
+    q = rng.standard_normal(d) * 3
+    keys = rng.standard_normal((n, d)) * 2
+    vals = rng.standard_normal((n, d))
+    dq, dk, dv = np.zeros(d), np.zeros((n, d)), np.zeros((n, d))
+    flips = [(0,), (2,)] if which == "q" else [(1, 0), (3, 2), (4, 1)]
+    target = {"q": dq, "k": dk, "v": dv}[which]
+    for idx in flips:
+        target[idx] = 0.05 * (1 if len(idx) % 2 else -1)
+
+    def out(qq, kk, vv):
+        s = kk @ qq
+        e = np.exp(s - s.max())
+        return (e / e.sum()) @ vv
+
+    base = out(q, keys, vals)
+    s = keys @ q
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    bound = oatt._row_slack(q, dq, keys, dk, vals, dv, p, base, 1.0)
+    worst = np.zeros(d)
+    import itertools
+    for mask in itertools.product([0, 1], repeat=len(flips)):
+        qq, kk, vv = q.copy(), keys.copy(), vals.copy()
+        t = {"q": qq, "k": kk, "v": vv}[which]
+        for m_, idx in zip(mask, flips):
+            if m_:
+                t[idx] += target[idx]
+        worst = np.maximum(worst, np.abs(out(qq, kk, vv) - base))
+    assert np.all(worst <= bound + 1e-15), (worst, bound)
+    assert np.all(bound <= 50 * worst + 1e-12)
