@@ -174,12 +174,37 @@ canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C
 }
 
 // ------------------------------------------------------------------ attention layout
-struct AttnLayout {
-  size_t proj_q, proj_k, proj_v, gemm, qp, kc, vc, kt, ks, vs, total;
+struct AttnPlan {
+  int Tpad, q_tiles, dv_parts, nsplit;
 };
 
-AttnLayout attn_layout(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix, int layer_type) {
+AttnPlan plan_attn(int dtype, int B, int C, int Hq, int Hkv, int d, int max_prefix, int layer_type, int window) {
+  AttnPlan p;
+  const int G = Hq / Hkv;
+  p.Tpad = attn_tail_rows(C);
+  p.q_tiles = (G * C + kAttnBM - 1) / kAttnBM;
+  p.dv_parts = d > 256 ? d / 256 : 1;
+  p.nsplit = 1;
+  if (dtype == CANVAS_BF16) {
+    // enough CTAs to fill the SMs, at least two key blocks per split
+    const int units = B * Hkv * p.q_tiles * p.dv_parts;
+    int keys = max_prefix;
+    if (layer_type == CANVAS_LAYER_SLIDING && window > 0) keys = std::min(keys, window + kAttnBM + 64);
+    keys += 64 + p.Tpad;
+    const int nblk = (keys + kAttnBN - 1) / kAttnBN;
+    p.nsplit = std::max(1, std::min(kNumSms / std::max(1, units), nblk / 2));
+  }
+  return p;
+}
+
+struct AttnLayout {
+  size_t proj_q, proj_k, proj_v, gemm, qp, kx, vx, vs_tail, kt, vs_pre, part_o, part_ml, total;
+};
+
+AttnLayout attn_layout(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix, int layer_type,
+                       int window) {
   AttnLayout L;
+  const AttnPlan pl = plan_attn(dtype, B, C, Hq, Hkv, d, max_prefix, layer_type, window);
   const size_t M = size_t(B) * C;
   const size_t es = dtype == CANVAS_BF16 ? 2 : 4;
   const bool global = layer_type == CANVAS_LAYER_GLOBAL;
@@ -190,15 +215,18 @@ AttnLayout attn_layout(int dtype, int B, int C, int D, int Hq, int Hkv, int d, i
   if (dtype == CANVAS_BF16) {
     L.gemm = std::max(gemm_ws_bytes(plan_gemm(int(M), Hq * d, D)), gemm_ws_bytes(plan_gemm(int(M), Hkv * d, D)));
   }
+  const size_t BH = size_t(B) * Hkv;
   L.qp = M * Hq * d * es;
-  L.kc = M * Hkv * d * es;
-  L.vc = global ? 0 : M * Hkv * d * es;
-  const size_t Lk = size_t(max_prefix) + C;
-  L.kt = global ? size_t(B) * Hkv * Lk * d * es : 0;
-  L.ks = global ? size_t(B) * Hkv * Lk * 4 : 0;
-  L.vs = L.ks;
+  L.kx = BH * pl.Tpad * d * es;
+  L.vx = L.kx;
+  L.vs_tail = global ? BH * pl.Tpad * 4 : 0;
+  L.kt = global ? BH * max_prefix * d * es : 0;
+  L.vs_pre = global ? BH * max_prefix * 4 : 0;
+  L.part_o = pl.nsplit > 1 ? size_t(pl.nsplit) * BH * pl.q_tiles * kAttnBM * d * 4 : 0;
+  L.part_ml = pl.nsplit > 1 ? size_t(pl.nsplit) * BH * pl.q_tiles * kAttnBM * 2 * 4 : 0;
   L.total = align_up(L.proj_q) + align_up(L.proj_k) + align_up(L.proj_v) + align_up(L.gemm) + align_up(L.qp) +
-            align_up(L.kc) + align_up(L.vc) + align_up(L.kt) + align_up(L.ks) + align_up(L.vs) + kAlign;
+            align_up(L.kx) + align_up(L.vx) + align_up(L.vs_tail) + align_up(L.kt) + align_up(L.vs_pre) +
+            align_up(L.part_o) + align_up(L.part_ml) + kAlign;
   return L;
 }
 
@@ -285,7 +313,7 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
 size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix,
                                        int layer_type) {
   if (!attn_shape_ok(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type)) return 0;
-  return attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type).total;
+  return attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type, 0).total;  // window 0: the largest plan
 }
 
 canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, const void* W_q, const void* W_k,
@@ -310,8 +338,13 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
                          (long long)kv->max_pages_per_seq * kv->page_tokens < max_prefix))
     return fail(CANVAS_ERR_ARG, "canvas_attention: cache geometry cannot hold max_prefix tokens");
   if (d % 64 != 0 || d > 512) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: head_dim must be 64, 128, ..., 512");
+  if (bf16 && (d & (d - 1)) != 0)
+    return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: bf16 head_dim must be 64, 128, 256 or 512");
   if (bf16 && D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: d_model must be a multiple of 8");
-  const AttnLayout L = attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type);
+  if (bf16 && max_prefix > 0 && kv->page_tokens % 64 != 0)
+    return fail(CANVAS_ERR_UNSUPPORTED, "canvas_attention: bf16 page_tokens must be a multiple of 64");
+  const AttnPlan pl = plan_attn(dtype, B, C, Hq, Hkv, d, max_prefix, layer_type, window);
+  const AttnLayout L = attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type, window);
   if (!ws_ok(workspace, ws_bytes, L.total))
     return fail(CANVAS_ERR_WORKSPACE, "canvas_attention: workspace missing, small or misaligned (need %zu)", L.total);
 
@@ -321,12 +354,15 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   float* proj_v = cv.take<float>(L.proj_v);
   void* gws = cv.take<char>(L.gemm);
   void* Qp = cv.take<char>(L.qp);
-  void* Kc = cv.take<char>(L.kc);
-  void* Vc = cv.take<char>(L.vc);
+  void* Kx = cv.take<char>(L.kx);
+  void* Vx = cv.take<char>(L.vx);
+  float* vs_tail = cv.take<float>(L.vs_tail);
   void* Kt = cv.take<char>(L.kt);
-  float* ks = cv.take<float>(L.ks);
-  float* vs = cv.take<float>(L.vs);
+  float* vs_pre = cv.take<float>(L.vs_pre);
+  float* part_o = cv.take<float>(L.part_o);
+  float* part_ml = cv.take<float>(L.part_ml);
   const int M = B * C;
+  const int G = Hq / Hkv;
 
   // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
   mark_start(CANVAS_KERNEL_PREP, stream);
@@ -344,7 +380,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     CANVAS_CUDA(launch_gemm_simt(x, W_k, 0, false, proj_k, M, Hkv * d, D, 0, stream));
     if (!global) CANVAS_CUDA(launch_gemm_simt(x, W_v, 0, false, proj_v, M, Hkv * d, D, 0, stream));
   }
-  // 2. rms + rotate of the canvas rows
+  // 2. rms + rotate of the canvas rows (queries, canvas keys / values)
   PrologueArgs p;
   p.proj_q = proj_q;
   p.proj_k = proj_k;
@@ -358,66 +394,124 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.d = d;
+  p.Tpad = pl.Tpad;
   p.eps = eps;
   p.global = global ? 1 : 0;
   p.Qp = Qp;
-  p.Kc = Kc;
-  p.Vc = Vc;
+  p.Kx = Kx;
+  p.Vx = Vx;
+  p.vs_tail = vs_tail;
   CANVAS_CUDA(launch_prologue(p, bf16, stream));
-  // 3. global layers: rotated raw rows + norm scalars of every key
-  if (global) {
-    KeyPrepArgs k;
-    k.pool = kv->k_pool;
-    k.block_table = kv->block_table;
-    k.max_pages = kv->max_pages_per_seq;
-    k.page_tokens = kv->page_tokens;
-    k.num_pages = kv->num_pages;
-    k.Rc = Kc;
-    k.gamma_k = gamma_k;
-    k.freq = freq;
-    k.prefix_len = prefix_len;
-    k.B = B;
-    k.C = C;
-    k.Hkv = Hkv;
-    k.d = d;
-    k.max_prefix = max_prefix;
-    k.eps = eps;
-    k.Kt = Kt;
-    k.ks = ks;
-    k.vs = vs;
-    CANVAS_CUDA(launch_key_prep(k, bf16, stream));
-  }
+  // 3. prefix keys of global layers, the prefix rows of the tail, zero padding
+  KeyPrepArgs k;
+  k.k_pool = kv->k_pool;
+  k.v_pool = kv->v_pool;
+  k.block_table = kv->block_table;
+  k.max_pages = kv->max_pages_per_seq;
+  k.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;
+  k.num_pages = kv->num_pages;
+  k.gamma_k = gamma_k;
+  k.freq = freq;
+  k.prefix_len = prefix_len;
+  k.B = B;
+  k.C = C;
+  k.Hkv = Hkv;
+  k.d = d;
+  k.max_prefix = max_prefix;
+  k.Tpad = pl.Tpad;
+  k.eps = eps;
+  k.global = global ? 1 : 0;
+  k.Kt = Kt;
+  k.vs_pre = vs_pre;
+  k.Kx = Kx;
+  k.Vx = Vx;
+  k.vs_tail = vs_tail;
+  CANVAS_CUDA(launch_key_prep(k, bf16, stream));
   mark_stop(CANVAS_KERNEL_PREP, stream);
+
   // 4. attention
-  AttnArgs a;
-  a.Qp = Qp;
-  a.k_pool = kv->k_pool;
-  a.v_pool = kv->v_pool;
-  a.block_table = kv->block_table;
-  a.max_pages = kv->max_pages_per_seq;
-  a.page_tokens = kv->page_tokens;
-  a.num_pages = kv->num_pages;
-  a.Kc = Kc;
-  a.Vc = Vc;
-  a.Kt = Kt;
-  a.ks = ks;
-  a.vs = vs;
-  a.prefix_len = prefix_len;
-  a.B = B;
-  a.C = C;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.d = d;
-  a.max_prefix = max_prefix;
-  a.window = window;
-  a.global = global ? 1 : 0;
-  a.v_unit_rms = v_unit_rms ? 1 : 0;
-  a.scale = scale;
-  a.out = out;
-  a.lse = lse;
-  mark_start(CANVAS_KERNEL_ATTENTION, stream);
-  CANVAS_CUDA(launch_attention_simt(a, bf16, stream));
-  mark_stop(CANVAS_KERNEL_ATTENTION, stream);
+  if (bf16) {
+    const uint64_t BH = uint64_t(B) * Hkv;
+    AttnTcMaps maps;
+    canvas_status st = make_map_bf16(&maps.q, Qp, BH * G * C, d, kAttnBM, 64);
+    if (st != CANVAS_OK) return st;
+    st = make_map_bf16(&maps.kx, Kx, BH * pl.Tpad, d, 64, 64);
+    if (st != CANVAS_OK) return st;
+    st = make_map_bf16(&maps.vx, Vx, BH * pl.Tpad, d, 64, 64);
+    if (st != CANVAS_OK) return st;
+    if (max_prefix > 0) {
+      const uint64_t pool_rows = uint64_t(kv->num_pages) * Hkv * kv->page_tokens;
+      st = global ? make_map_bf16(&maps.kpre, Kt, BH * max_prefix, d, 64, 64)
+                  : make_map_bf16(&maps.kpre, kv->k_pool, pool_rows, d, 64, 64);
+      if (st != CANVAS_OK) return st;
+      st = make_map_bf16(&maps.vpre, global ? kv->k_pool : kv->v_pool, pool_rows, d, 64, 64);
+      if (st != CANVAS_OK) return st;
+    } else {
+      maps.kpre = maps.kx;  // never read: no prefix sub-blocks
+      maps.vpre = maps.vx;
+    }
+    AttnTcArgs t;
+    t.B = B;
+    t.C = C;
+    t.Hq = Hq;
+    t.Hkv = Hkv;
+    t.G = G;
+    t.d = d;
+    t.DV = d > 256 ? 256 : d;
+    t.dv_parts = pl.dv_parts;
+    t.q_tiles = pl.q_tiles;
+    t.nsplit = pl.nsplit;
+    t.max_prefix = max_prefix;
+    t.window = global ? 0 : window;
+    t.Tpad = pl.Tpad;
+    t.kpre_paged = global ? 0 : 1;
+    t.block_table = kv->block_table;
+    t.max_pages = kv->max_pages_per_seq;
+    t.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;
+    t.num_pages = kv->num_pages;
+    t.prefix_len = prefix_len;
+    t.vs_pre = v_unit_rms ? vs_pre : nullptr;
+    t.vs_tail = v_unit_rms ? vs_tail : nullptr;
+    t.c_log2 = scale * 1.4426950408889634f;
+    t.out = static_cast<__nv_bfloat16*>(out);
+    t.lse = lse;
+    t.part_o = part_o;
+    t.part_ml = part_ml;
+    mark_start(CANVAS_KERNEL_ATTENTION, stream);
+    CANVAS_CUDA(launch_attention_tc(maps, t, stream));
+    if (t.nsplit > 1) CANVAS_CUDA(launch_attention_combine(t, stream));
+    mark_stop(CANVAS_KERNEL_ATTENTION, stream);
+  } else {
+    AttnArgs a;
+    a.Qp = Qp;
+    a.k_pre = global ? Kt : kv->k_pool;
+    a.v_pre = global ? kv->k_pool : kv->v_pool;
+    a.block_table = kv->block_table;
+    a.max_pages = kv->max_pages_per_seq;
+    a.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;
+    a.num_pages = kv->num_pages;
+    a.Kx = Kx;
+    a.Vx = Vx;
+    a.vs_pre = vs_pre;
+    a.vs_tail = vs_tail;
+    a.prefix_len = prefix_len;
+    a.B = B;
+    a.C = C;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.max_prefix = max_prefix;
+    a.window = window;
+    a.Tpad = pl.Tpad;
+    a.global = global ? 1 : 0;
+    a.v_unit_rms = v_unit_rms ? 1 : 0;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    mark_start(CANVAS_KERNEL_ATTENTION, stream);
+    CANVAS_CUDA(launch_attention_simt(a, bf16, stream));
+    mark_stop(CANVAS_KERNEL_ATTENTION, stream);
+  }
   return CANVAS_OK;
 }
 

@@ -1,12 +1,15 @@
 // attention_simt.cu -- decode-mode canvas attention on CUDA cores (fp32 math).
 //
-// The fp32 variant of the step runs here; it also serves shapes the tcgen05
-// kernel does not take.  One CTA per (sequence b, KV head, canvas row i): its
-// G warps are the G query heads that share the KV head (GQA), and all of them
-// see the same key set -- the visible prefix keys of row i (sliding window or
-// whole prefix) followed by all C canvas keys.  Keys and values are staged in
-// shared memory 32 (or 16) rows at a time; each warp keeps an online softmax
-// (lane = key for scores, lane = channel for the output).
+// The fp32 variant of the step runs here.  One CTA per (sequence b, KV head,
+// canvas row i): its G warps are the G query heads that share the KV head
+// (GQA), and all of them see the same key set -- the visible prefix keys of
+// row i (sliding window or whole prefix) followed by all C canvas keys, i.e.
+// the contiguous position range [lo, P + C).  Positions below P64 come from
+// the committed prefix in place (paged cache, or the prepared global keys),
+// positions from P64 on from the dense tail buffers (kernels.h).  Keys and
+// values are staged in shared memory 32 (or 16) rows at a time; each warp
+// keeps an online softmax (lane = key for scores, lane = channel for the
+// output).
 //
 // Method: AI Trends summary of a DiffusionGemma 26B notebook
 // (aitrends.kr/articles/94089), "섹션별 상세", decode mode (the canvas attends
@@ -36,20 +39,16 @@ __global__ void __launch_bounds__(1024) attention_simt_kernel(AttnArgs a) {
   float* sK = sm;                       // [KB][d + 1]
   float* sV = sK + KB * (d + 1);        // [KB][d]
   float* sQ = sV + KB * d;              // [G][d]
-  float* sS = sQ + G * d;               // [KB] key scale (global layers)
-  float* sVS = sS + KB;                 // [KB] value scale
 
   const int P = a.prefix_len[b];
-  if (P < 0 || P > a.max_prefix) {
-    if (threadIdx.x == 0 && i == 0 && hk == 0) record_error(CANVAS_ERR_BOUNDS);
-    return;
-  }
+  if (P < 0 || P > a.max_prefix) return;  // reported by the key-prep kernel
+  const int P64 = P & ~63;
   const int lo = (a.global || a.window <= 0) ? 0 : max(0, P + i - a.window);
-  const int n_pre = P - lo, n_keys = n_pre + a.C;
-  const int L = a.max_prefix + a.C;
+  const int n_keys = P + a.C - lo;
+  const size_t grp = (size_t)b * a.Hkv + hk;
 
   // this warp's query row
-  const T* q = static_cast<const T*>(a.Qp) + ((((size_t)b * a.Hkv + hk) * G + warp) * a.C + i) * d;
+  const T* q = static_cast<const T*>(a.Qp) + (((grp * G + warp) * a.C) + i) * d;
   for (int t = lane; t < d; t += 32) sQ[warp * d + t] = to_f32(q[t]);
 
   const int per = d / 32;  // channels per lane (d <= 512)
@@ -64,39 +63,29 @@ __global__ void __launch_bounds__(1024) attention_simt_kernel(AttnArgs a) {
     // stage KB keys / values as fp32
     for (int e = threadIdx.x; e < KB * d; e += nthr) {
       const int r = e / d, t = e % d;
-      float kv = 0.f, vv = 0.f, ks = 1.f, vsc = 1.f;
+      float kv = 0.f, vv = 0.f;
       if (r < nk) {
-        const int kk = k0 + r;  // index in this row's key list
-        const bool pre = kk < n_pre;
-        const int j = pre ? lo + kk : (kk - n_pre);  // prefix position / canvas index
-        if (a.global) {
-          const size_t krow = ((size_t)b * a.Hkv + hk) * L + (pre ? j : P + j);
-          kv = to_f32(static_cast<const T*>(a.Kt)[krow * d + t]);
-          ks = a.ks[krow];
-          vsc = a.v_unit_rms ? a.vs[krow] : 1.f;
-          const T* vr = pre ? page_row<T>(a, a.k_pool, b, hk, j)
-                            : static_cast<const T*>(a.Kc) + (((size_t)b * a.Hkv + hk) * a.C + j) * d;
-          if (vr == nullptr) {
-            if (t == 0) record_error(CANVAS_ERR_BOUNDS);
-          } else {
-            vv = to_f32(vr[t]);
-          }
+        const int pos = lo + k0 + r;
+        const T *kr, *vr;
+        float vsc = 1.f;
+        if (pos < P64) {
+          kr = a.global ? static_cast<const T*>(a.k_pre) + (grp * a.max_prefix + pos) * d
+                        : page_row<T>(a, a.k_pre, b, hk, pos);
+          vr = page_row<T>(a, a.v_pre, b, hk, pos);
+          if (a.v_unit_rms) vsc = a.vs_pre[grp * a.max_prefix + pos];
         } else {
-          const T* kr = pre ? page_row<T>(a, a.k_pool, b, hk, j)
-                            : static_cast<const T*>(a.Kc) + (((size_t)b * a.Hkv + hk) * a.C + j) * d;
-          const T* vr = pre ? page_row<T>(a, a.v_pool, b, hk, j)
-                            : static_cast<const T*>(a.Vc) + (((size_t)b * a.Hkv + hk) * a.C + j) * d;
-          if (kr == nullptr || vr == nullptr) {
-            if (t == 0) record_error(CANVAS_ERR_BOUNDS);
-          } else {
-            kv = to_f32(kr[t]);
-            vv = to_f32(vr[t]);
-          }
+          const size_t trow = grp * a.Tpad + (pos - P64);
+          kr = static_cast<const T*>(a.Kx) + trow * d;
+          vr = static_cast<const T*>(a.Vx) + trow * d;
+          if (a.v_unit_rms) vsc = a.vs_tail[trow];
+        }
+        if (kr != nullptr && vr != nullptr) {  // a bad page id is reported by the key-prep kernel
+          kv = to_f32(kr[t]);
+          vv = to_f32(vr[t]) * vsc;
         }
       }
       sK[r * (d + 1) + t] = kv;
-      sV[r * d + t] = vv * vsc;
-      if (t == 0) sS[r] = ks;
+      sV[r * d + t] = vv;
     }
     __syncthreads();
     // scores: lane = key
@@ -108,14 +97,14 @@ __global__ void __launch_bounds__(1024) attention_simt_kernel(AttnArgs a) {
         const float* kr = sK + r * (d + 1);
         const float* qr = sQ + warp * d;
         for (int t = 0; t < d; ++t) acc = fmaf(qr[t], kr[t], acc);
-        s = acc * sS[r] * a.scale;
+        s = acc * a.scale;
       }
       float bm = s;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
       const float mn = fmaxf(m, bm);
-      const float alpha = (m == -INFINITY) ? 0.f : __expf(m - mn);
-      const float p = (r < nk) ? __expf(s - mn) : 0.f;
+      const float alpha = (m == -INFINITY) ? 0.f : expf(m - mn);
+      const float p = (r < nk) ? expf(s - mn) : 0.f;
       float ps = p;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
@@ -152,7 +141,7 @@ __global__ void __launch_bounds__(1024) attention_simt_kernel(AttnArgs a) {
 template <typename T, int KB>
 cudaError_t launch_kb(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
-  const size_t smem = sizeof(float) * (size_t(KB) * (a.d + 1) + size_t(KB) * a.d + size_t(G) * a.d + 2 * KB);
+  const size_t smem = sizeof(float) * (size_t(KB) * (a.d + 1) + size_t(KB) * a.d + size_t(G) * a.d);
   cudaError_t e = cudaFuncSetAttribute(attention_simt_kernel<T, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
   if (e != cudaSuccess) return e;

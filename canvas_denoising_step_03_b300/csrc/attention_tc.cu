@@ -1,0 +1,580 @@
+// attention_tc.cu -- decode-mode canvas attention on the 5th-generation
+// tensor cores (tcgen05, TMEM accumulators, TMA-fed shared memory).
+//
+// Method: AI Trends summary of a DiffusionGemma 26B notebook
+// (aitrends.kr/articles/94089), "섹션별 상세": decode mode (the canvas attends
+// bidirectionally to the committed prefix in the KV cache and to the whole
+// canvas), scores q . k with the scale fixed by the scalar QK norm; the
+// glossary entries on sliding-window attention and on the shared K/V
+// projection of full-attention layers.
+//
+// Work unit (one CTA): a 128-row query tile of one (sequence b, KV head hk)
+// -- the G query heads of the KV head packed as rows g * C + i (GQA) -- one
+// part of the value dimension (DV = min(d, 256) columns) and one contiguous
+// range of 128-key blocks (a KV split).  Keys are the position range of the
+// key sequence (kernels.h); 64-key sub-blocks come either from the committed
+// prefix in place (paged cache through the block table, or the dense global
+// keys) or from the dense tail buffers.
+//
+// Roles (192 threads):
+//   warp 0       TMA producer: Q tile once; then K chunks and V sub-blocks in
+//                the order the MMA warp consumes them, through a ring of
+//                32 KB stages (128-byte swizzle).
+//   warp 1       TMEM allocation (512 columns) and the MMA issuer:
+//                S_n = Q K_n^T (M=128, N=128, both operands in shared memory)
+//                into one of two S buffers; O += P_n V_n (M=128, N=DV, P read
+//                from TMEM where the softmax wrote it over S_n, V from shared
+//                memory, MN-major).  Issue order QK0 QK1 PV0 QK2 PV1 ...
+//   warps 2..5   softmax and epilogue, one query row per thread (TMEM lane):
+//                S from TMEM, masking, running max in the log2 domain,
+//                P = 2^(S c - m) rounded to bf16 and stored back to TMEM.
+//                The accumulator is rescaled only when the running max grows
+//                by more than 8 (P stays below 2^8), so most blocks never
+//                touch O.
+// With d = 512 the 128 x 512 fp32 accumulator would fill all of TMEM, so the
+// value dimension is split across two CTAs (DV = 256 each) that both form
+// the full S; every other shape keeps the whole row in one CTA.
+// Results: bf16 rows (and the natural-log LSE) when the key range is not
+// split, else fp32 partial rows plus (max, sum) for the combine kernel.
+// Every mbarrier wait is bounded (common.cuh).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace canvas {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kStageBytes = 32768;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct Cfg {
+  static constexpr int DV = D < 256 ? D : 256;
+  static constexpr int NCH = D / 64;             // 64-wide chunks of the head dimension
+  static constexpr int KCH = NCH < 2 ? NCH : 2;  // chunks per K stage
+  static constexpr int KST = NCH / KCH;          // K stages per block
+  static constexpr int NST = D == 512 ? 3 : 4;   // ring stages
+  static constexpr int QBytes = NCH * 16384;
+  static constexpr int Smem = QBytes + NST * kStageBytes + 1024 + 256;
+};
+
+// The block sequence of one CTA (identical in every thread).
+struct Seq {
+  int P, P64, T, s0, n_pre, n_sub, kb0, nb, lo_max;
+  bool ok;
+};
+
+// First visible prefix position of canvas row i (the host passes window 0 on
+// global layers: the whole prefix is visible).
+__device__ __forceinline__ int window_lo(const AttnTcArgs& a, int P, int i) {
+  if (a.window <= 0) return 0;
+  return min(P, max(0, P + i - a.window));
+}
+
+__device__ __forceinline__ Seq make_seq(const AttnTcArgs& a, int b, int qt, int split) {
+  Seq q;
+  q.P = a.prefix_len[b];
+  q.ok = q.P >= 0 && q.P <= a.max_prefix;
+  if (!q.ok) return q;
+  q.P64 = q.P & ~63;
+  q.T = q.P - q.P64 + a.C;
+  const int GC = a.G * a.C;
+  const int R0 = qt * kAttnBM;
+  const int nrows = min(kAttnBM, GC - R0);
+  int i_min, i_max;
+  if (R0 / a.C == (R0 + nrows - 1) / a.C) {
+    i_min = R0 % a.C;
+    i_max = (R0 + nrows - 1) % a.C;
+  } else {
+    i_min = 0;
+    i_max = a.C - 1;
+  }
+  const int lo_min = window_lo(a, q.P, i_min);
+  q.lo_max = window_lo(a, q.P, i_max);
+  q.s0 = lo_min & ~63;
+  q.n_pre = (q.P64 - q.s0) / 64;
+  q.n_sub = q.n_pre + (q.T + 63) / 64;
+  const int nblk = (q.n_sub + 1) / 2;
+  q.kb0 = (int)((long long)split * nblk / a.nsplit);
+  q.nb = (int)((long long)(split + 1) * nblk / a.nsplit) - q.kb0;
+  return q;
+}
+
+// TMA row of 64-key sub-block s in the prefix (paged pool) or tail buffers.
+__device__ __forceinline__ int paged_row(const AttnTcArgs& a, int b, int hk, int pos) {
+  const int lp = pos / a.page_tokens;
+  int page = lp < a.max_pages ? a.block_table[(size_t)b * a.max_pages + lp] : -1;
+  if (page < 0 || page >= a.num_pages) {
+    record_error(CANVAS_ERR_BOUNDS);
+    page = 0;  // stay inside the pool; the call reports the error
+  }
+  return (page * a.Hkv + hk) * a.page_tokens + pos % a.page_tokens;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_tc_kernel(const __grid_constant__ AttnTcMaps maps, AttnTcArgs a) {
+  using K = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* ring = smem + K::QBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + K::NST * kStageBytes);
+  uint64_t* empty = full + K::NST;
+  uint64_t* q_full = empty + K::NST;
+  uint64_t* s_full = q_full + 1;   // [2]
+  uint64_t* p_full = s_full + 2;   // [2]
+  uint64_t* pv_done = p_full + 2;  // [2]
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int x = blockIdx.x;
+  const int dvp = x % a.dv_parts;
+  x /= a.dv_parts;
+  const int qt = x % a.q_tiles;
+  x /= a.q_tiles;
+  const int split = x % a.nsplit;
+  x /= a.nsplit;
+  const int hk = x % a.Hkv;
+  const int b = x / a.Hkv;
+  const int grp = b * a.Hkv + hk;
+  const Seq sq = make_seq(a, b, qt, split);
+  if (!sq.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(CANVAS_ERR_BOUNDS);
+    return;  // uniform: before any barrier or TMEM allocation
+  }
+  const int nb = sq.nb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < K::NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&p_full[j], 128);
+      mbar_init(&pv_done[j], 1);
+    }
+    mbar_init(drain, 1);
+    flags[0] = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&maps.q);
+    tma_prefetch_desc(&maps.kpre);
+    tma_prefetch_desc(&maps.vpre);
+    tma_prefetch_desc(&maps.kx);
+    tma_prefetch_desc(&maps.vx);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(q_full, uint32_t(K::QBytes));
+      const int qrow = grp * a.G * a.C + qt * kAttnBM;
+      for (int c = 0; c < K::NCH; ++c) tma_load_2d(sQ + c * 16384, &maps.q, q_full, c * 64, qrow);
+      int it = 0;
+      bool alive = true;
+      auto acquire = [&](uint32_t bytes) -> uint8_t* {
+        const int s = it % K::NST;
+        if (!mbar_wait(&empty[s], ((it / K::NST) & 1) ^ 1, flags)) {
+          alive = false;
+          return nullptr;
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        ++it;
+        return ring + s * kStageBytes;
+      };
+      auto k_row = [&](int s, const CUtensorMap*& map) -> int {
+        if (s < sq.n_pre) {
+          const int pos = sq.s0 + 64 * s;
+          map = &maps.kpre;
+          return a.kpre_paged ? paged_row(a, b, hk, pos) : grp * a.max_prefix + pos;
+        }
+        map = &maps.kx;
+        return grp * a.Tpad + 64 * (s - sq.n_pre);
+      };
+      auto v_row = [&](int s, const CUtensorMap*& map) -> int {
+        if (s < sq.n_pre) {
+          map = &maps.vpre;
+          return paged_row(a, b, hk, sq.s0 + 64 * s);
+        }
+        map = &maps.vx;
+        return grp * a.Tpad + 64 * (s - sq.n_pre);
+      };
+      auto load_k = [&](int n) {
+        const int kb = sq.kb0 + n;
+        for (int ks = 0; ks < K::KST && alive; ++ks) {
+          uint8_t* dst = acquire(uint32_t(K::KCH * 16384));
+          if (!dst) break;
+          for (int u = 0; u < 2; ++u) {
+            const CUtensorMap* map;
+            const int row = k_row(2 * kb + u, map);
+            for (int c = 0; c < K::KCH; ++c)
+              tma_load_2d(dst + c * 16384 + u * 8192, map, &full[(it - 1) % K::NST], (ks * K::KCH + c) * 64, row);
+          }
+        }
+      };
+      auto load_v = [&](int n) {
+        const int kb = sq.kb0 + n;
+        for (int u = 0; u < 2 && alive; ++u) {
+          uint8_t* dst = acquire(uint32_t(K::DV / 64 * 8192));
+          if (!dst) break;
+          const CUtensorMap* map;
+          const int row = v_row(2 * kb + u, map);
+          for (int c = 0; c < K::DV / 64; ++c)
+            tma_load_2d(dst + c * 8192, map, &full[(it - 1) % K::NST], dvp * K::DV + c * 64, row);
+        }
+      };
+      for (int n = 0; n < nb && alive; ++n) {
+        load_k(n);
+        if (n >= 1) load_v(n - 1);
+      }
+      if (nb >= 1 && alive) load_v(nb - 1);
+      // drain: every load this thread issued has landed before the CTA exits
+      volatile int no_abort = 0;
+      mbar_wait(q_full, 0, &no_abort);
+      for (int j = max(0, it - K::NST); j < it; ++j) mbar_wait(&full[j % K::NST], (j / K::NST) & 1, &no_abort);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc_qk = idesc_bf16_f32(128, kAttnBN, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, K::DV, 0, 1);
+      const uint32_t q_base = smem_u32(sQ);
+      int it = 0;
+      bool alive = mbar_wait(q_full, 0, flags);
+      tc_fence_after();
+      auto consume = [&]() -> uint32_t {
+        const int s = it % K::NST;
+        if (!mbar_wait(&full[s], (it / K::NST) & 1, flags)) {
+          alive = false;
+          return 0;
+        }
+        tc_fence_after();
+        ++it;
+        return smem_u32(ring + s * kStageBytes);
+      };
+      auto qk = [&](int n) {
+        const uint32_t tS = tmem + 256 + (n & 1) * 128;
+        for (int ks = 0; ks < K::KST && alive; ++ks) {
+          const uint32_t st = consume();
+          if (!alive) return;
+#pragma unroll
+          for (int c = 0; c < K::KCH; ++c) {
+            const int ch = ks * K::KCH + c;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(q_base + ch * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(st + c * 16384 + kk * 32, 16, 1024);
+              mma_bf16_ss(tS, ad, bd, idesc_qk, (ch | kk) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&empty[(it - 1) % K::NST]);
+        }
+        mma_commit(&s_full[n & 1]);
+      };
+      auto pv = [&](int n) {
+        const uint32_t tS = tmem + 256 + (n & 1) * 128;
+        for (int u = 0; u < 2 && alive; ++u) {
+          const uint32_t st = consume();
+          if (!alive) return;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = smem_desc_sw128(st + kk * 2048, 8192, 1024);
+            mma_bf16_ts(tmem, tS + u * 32 + kk * 8, bd, idesc_pv, (n | u | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[(it - 1) % K::NST]);
+        }
+        mma_commit(&pv_done[n & 1]);
+      };
+      if (alive && nb >= 1) qk(0);
+      if (alive && nb >= 2) qk(1);
+      for (int n = 0; n < nb && alive; ++n) {
+        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, flags)) break;
+        tc_fence_after();
+        pv(n);
+        if (n + 2 < nb) qk(n + 2);
+      }
+      // every MMA issued has completed before TMEM is released
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue
+    const int quad = warp & 3;
+    const int lrow = quad * 32 + lane;
+    const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    const int GC = a.G * a.C;
+    const int R = qt * kAttnBM + lrow;
+    const bool valid = R < GC;
+    const int g = valid ? R / a.C : 0, i = valid ? R % a.C : 0;
+    const int lo_row = valid ? window_lo(a, sq.P, i) : 0;
+    float m_run = -INFINITY, l = 0.f;
+    bool alive = true;
+    for (int n = 0; n < nb; ++n) {
+      if (!mbar_wait(&s_full[n & 1], (n >> 1) & 1, flags)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + 256 + (n & 1) * 128;
+      // visibility of the block's 128 keys: a uniform test first, per-key bits otherwise
+      const int kb = sq.kb0 + n;
+      bool clean = true;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int sb = 2 * kb + u;
+        if (sb < sq.n_pre) {
+          clean = clean && (sq.s0 + 64 * sb >= sq.lo_max);
+        } else {
+          const int t0 = 64 * (sb - sq.n_pre);
+          clean = clean && (t0 + 64 <= sq.T) && (sq.P64 + t0 >= sq.lo_max || sq.P64 + t0 >= sq.P);
+        }
+      }
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (!clean) {
+        for (int c = 0; c < kAttnBN; ++c) {
+          const int sb = 2 * kb + (c >> 6), off = c & 63;
+          bool v;
+          if (sb < sq.n_pre) {
+            v = sq.s0 + 64 * sb + off >= lo_row;
+          } else {
+            const int t = 64 * (sb - sq.n_pre) + off;
+            const int pos = sq.P64 + t;
+            v = (t < sq.T) && (pos >= sq.P || pos >= lo_row);
+          }
+          if (!v) vis[c >> 5] &= ~(1u << (c & 31));
+        }
+      }
+      // pass 1: block maximum (log2 domain)
+      float bmax = -INFINITY;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(tS + c4 * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((vis[c4] >> j) & 1u) bmax = fmaxf(bmax, __uint_as_float(r[j]) * a.c_log2);
+      }
+      const float m_new = fmaxf(m_run, bmax);
+      const bool need = (m_run != -INFINITY) && (m_new > m_run + kRescaleLog2);
+      if (__any_sync(0xffffffffu, need)) {
+        // the previous block's P.V must have landed in O before it is rescaled
+        if (!mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = need ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < K::DV / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + cc * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(tmem + lane_off + cc * 32, r);
+        }
+        tmem_st_wait();
+      }
+      if (need) {
+        l *= exp2f(m_run - m_new);
+        m_run = m_new;
+      } else if (m_run == -INFINITY) {
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // pass 2: P = 2^(s c - m) rounded to bf16 pairs, written over the first
+      // 64 columns of S (keys 32 c4 .. 32 c4 + 31 -> columns 16 c4 .. 16 c4 + 15;
+      // those S columns were read in this or an earlier chunk)
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(tS + c4 * 32, r);
+        tmem_ld_wait();
+        const uint32_t vw = vis[c4];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x0 = ((vw >> (2 * j)) & 1u) ? __uint_as_float(r[2 * j]) * a.c_log2 - m_use : -INFINITY;
+          const float x1 = ((vw >> (2 * j + 1)) & 1u) ? __uint_as_float(r[2 * j + 1]) * a.c_log2 - m_use : -INFINITY;
+          const float p0 = exp2f(x0), p1 = exp2f(x1);
+          if (a.vs_pre == nullptr) {
+            pk[j] = pack_bf16x2(p0, p1);
+            // the sum uses the rounded weights, so O / l is an exact convex
+            // combination of value rows with the stored weights
+            l += bf16_bits_to_f32(pk[j] & 0xffffu) + bf16_bits_to_f32(pk[j] >> 16);
+          } else {
+            // unit-RMS values: weight of each key times its row scalar sc; the
+            // sum divides the stored product back by sc for the same reason
+            float sc[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ce = c4 * 32 + 2 * j + e, sb = 2 * kb + (ce >> 6), off = ce & 63;
+              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + sq.s0 + 64 * sb + off]
+                                    : a.vs_tail[(size_t)grp * a.Tpad + 64 * (sb - sq.n_pre) + off];
+            }
+            pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
+            const float w0 = bf16_bits_to_f32(pk[j] & 0xffffu), w1 = bf16_bits_to_f32(pk[j] >> 16);
+            l += (sc[0] > 0.f ? w0 / sc[0] : 0.f) + (sc[1] > 0.f ? w1 / sc[1] : 0.f);
+          }
+        }
+        tmem_st16(tS + c4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[n & 1]);
+    }
+    if (alive && nb >= 1) {
+      alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
+      tc_fence_after();
+    }
+    // ---------------- epilogue
+    if (alive) {
+      const int h = hk * a.G + g;
+      if (a.nsplit == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d + dvp * K::DV;
+        for (int cc = 0; cc < K::DV / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + cc * 32, r);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+            uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+        if (valid && dvp == 0 && a.lse != nullptr)
+          a.lse[((size_t)b * a.C + i) * a.Hq + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        const size_t prow = ((size_t)split * a.B * a.Hkv + grp) * (size_t)(a.q_tiles * kAttnBM) + qt * kAttnBM + lrow;
+        float* dst = a.part_o + prow * a.d + dvp * K::DV;
+        for (int cc = 0; cc < K::DV / 32; ++cc) {
+          uint32_t r[32];
+          if (nb >= 1) {
+            tmem_ld32(tmem + lane_off + cc * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          float4* o4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                                __uint_as_float(r[4 * j + 3]));
+        }
+        if (dvp == 0) {
+          a.part_ml[prow * 2] = m_run;
+          a.part_ml[prow * 2 + 1] = l;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One block of 128 threads per output row (b, KV head, packed row g*C + i):
+// merges the KV splits' partial rows by their running max and sum.
+__global__ void __launch_bounds__(128) attention_combine_kernel(AttnTcArgs a) {
+  const int GC = a.G * a.C;
+  const int row = blockIdx.x % GC;
+  const int grp = blockIdx.x / GC;
+  const int b = grp / a.Hkv, hk = grp % a.Hkv;
+  const int g = row / a.C, i = row % a.C;
+  const size_t rows_per_split = (size_t)a.B * a.Hkv * a.q_tiles * kAttnBM;
+  const size_t prow0 = (size_t)grp * a.q_tiles * kAttnBM + row;
+  float M = -INFINITY;
+  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.part_ml[(s * rows_per_split + prow0) * 2]);
+  float L = 0.f;
+  for (int s = 0; s < a.nsplit; ++s) {
+    const float ms = a.part_ml[(s * rows_per_split + prow0) * 2];
+    if (ms != -INFINITY) L += exp2f(ms - M) * a.part_ml[(s * rows_per_split + prow0) * 2 + 1];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int h = hk * a.G + g;
+  __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d;
+  for (int c = threadIdx.x * 2; c < a.d; c += 256) {
+    float o0 = 0.f, o1 = 0.f;
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float ms = a.part_ml[(s * rows_per_split + prow0) * 2];
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - M);
+      const float2 v = *reinterpret_cast<const float2*>(a.part_o + (s * rows_per_split + prow0) * a.d + c);
+      o0 = fmaf(w, v.x, o0);
+      o1 = fmaf(w, v.y, o1);
+    }
+    *reinterpret_cast<__nv_bfloat162*>(dst + c) = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+  }
+  if (threadIdx.x == 0 && a.lse != nullptr)
+    a.lse[((size_t)b * a.C + i) * a.Hq + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
+  static bool attr_set = false;
+  const int smem = Cfg<D>::Smem;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = a.B * a.Hkv * a.nsplit * a.q_tiles * a.dv_parts;
+  attention_tc_kernel<D><<<grid, kThreads, smem, stream>>>(maps, a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_tc_smem_bytes(int d) {
+  switch (d) {
+    case 64: return Cfg<64>::Smem;
+    case 128: return Cfg<128>::Smem;
+    case 256: return Cfg<256>::Smem;
+    case 512: return Cfg<512>::Smem;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_d<64>(maps, a, stream);
+    case 128: return launch_d<128>(maps, a, stream);
+    case 256: return launch_d<256>(maps, a, stream);
+    case 512: return launch_d<512>(maps, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream) {
+  const int grid = a.B * a.Hkv * a.G * a.C;
+  attention_combine_kernel<<<grid, 128, 0, stream>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace canvas

@@ -56,6 +56,24 @@ cudaError_t launch_gemm_simt(const void* A, const void* B, int b_mn_major, bool 
                              int K, int accumulate, cudaStream_t stream);
 
 // ----------------------------------------------------------------- attention
+//
+// Key sequence of one (sequence b, KV head).  Canvas row i sits at absolute
+// position P + i (P = prefix_len[b]); P64 = P rounded down to a multiple of 64.
+//   positions [0, P64)        committed prefix, read in place: the paged cache
+//                             (sliding layers, and values of global layers) or
+//                             the prepared key buffer Kt (global-layer keys);
+//   positions [P64, P + C)    the "tail": the last P - P64 prefix rows followed
+//                             by the C canvas rows, gathered into the dense
+//                             buffers Kx / Vx [B][Hkv][Tpad][d] (row t holds
+//                             position P64 + t; rows past P + C are zero).
+// Every 64-key sub-block is therefore either whole in the paged / prepared
+// prefix or whole in the tail buffers, and no tile ever reads a cache slot
+// that holds no token.
+
+// Tail rows: 64 * (ceil((C + 63) / 64) + 1), so a 128-key block that starts
+// inside the tail never reads past the buffer.
+inline int attn_tail_rows(int C) { return 64 * ((C + 63 + 63) / 64 + 1); }
+
 struct PrologueArgs {
   const float* proj_q;  // [B*C, Hq*d]
   const float* proj_k;  // [B*C, Hkv*d]
@@ -64,53 +82,80 @@ struct PrologueArgs {
   const float* gamma_k;
   const float* freq;
   const int32_t* prefix_len;
-  int B, C, Hq, Hkv, d;
+  int B, C, Hq, Hkv, d, Tpad;
   float eps;
   int global;
   void* Qp;  // [B][Hkv][G][C][d]
-  void* Kc;  // sliding: [B][Hkv][C][d] final canvas keys; global: raw canvas r
-  void* Vc;  // sliding: [B][Hkv][C][d] canvas values; global: unused
+  void* Kx;  // [B][Hkv][Tpad][d] keys of the tail rows
+  void* Vx;  // [B][Hkv][Tpad][d] values of the tail rows (global: raw r)
+  float* vs_tail;  // [B][Hkv][Tpad] global: sqrt(d) / (|r| + eps) of each tail row
 };
 cudaError_t launch_prologue(const PrologueArgs& p, bool bf16, cudaStream_t stream);
 
-// Global layers: per key row j of the key set (prefix then canvas), the
-// rotation of the raw row and its norm scalars.
+// Global-layer prefix keys Kt[j] = rotate(rms(r_j)) for j < P64, and the tail
+// rows [P64, P) of both layer types (copied, or prepared from raw r), and the
+// zero rows past the canvas.
 struct KeyPrepArgs {
-  const void* pool;          // raw r pages [num_pages][Hkv][pt][d]
+  const void* k_pool;        // [num_pages][Hkv][pt][d]: keys (sliding) / raw r (global)
+  const void* v_pool;        // values (sliding) or null
   const int32_t* block_table;
   int max_pages, page_tokens, num_pages;
-  const void* Rc;            // raw canvas r [B][Hkv][C][d]
   const float* gamma_k;
   const float* freq;
   const int32_t* prefix_len;
-  int B, C, Hkv, d, max_prefix;
+  int B, C, Hkv, d, max_prefix, Tpad;
   float eps;
-  void* Kt;                  // [B][Hkv][max_prefix + C][d] rotate(r)
-  float* ks;                 // [B][Hkv][max_prefix + C] gamma_k * sqrt(d) / (|r| + eps)
-  float* vs;                 // [B][Hkv][max_prefix + C] sqrt(d) / (|r| + eps)
+  int global;
+  void* Kt;                  // [B][Hkv][max_prefix][d] (global)
+  float* vs_pre;             // [B][Hkv][max_prefix] (global)
+  void* Kx;
+  void* Vx;
+  float* vs_tail;
 };
 cudaError_t launch_key_prep(const KeyPrepArgs& k, bool bf16, cudaStream_t stream);
 
+// CUDA-core attention (fp32 calls)
 struct AttnArgs {
   const void* Qp;            // [B][Hkv][G][C][d]
-  // sliding: prefix K/V from the pools; canvas K/V from Kc/Vc
-  // global : keys from Kt (+ks), values from the pool / Rc (+vs if v_unit_rms)
-  const void* k_pool;
-  const void* v_pool;
+  const void* k_pre;         // sliding: k pool (paged); global: Kt (dense)
+  const void* v_pre;         // paged pool: values (sliding) / raw r (global)
   const int32_t* block_table;
   int max_pages, page_tokens, num_pages;
-  const void* Kc;
-  const void* Vc;
-  const void* Kt;
-  const float* ks;
-  const float* vs;
+  const void* Kx;
+  const void* Vx;
+  const float* vs_pre;       // global + v_unit_rms: per-row value scale
+  const float* vs_tail;
   const int32_t* prefix_len;
-  int B, C, Hq, Hkv, d, max_prefix, window;
+  int B, C, Hq, Hkv, d, max_prefix, window, Tpad;
   int global, v_unit_rms;
   float scale;
   void* out;                 // [B][C][Hq*d]
   float* lse;                // [B][C][Hq] or null
 };
 cudaError_t launch_attention_simt(const AttnArgs& a, bool bf16, cudaStream_t stream);
+
+// tcgen05 attention (bf16 calls, d in {64, 128, 256, 512})
+constexpr int kAttnBM = 128;       // query rows per tile (TMEM lanes)
+constexpr int kAttnBN = 128;       // keys per block
+struct AttnTcArgs {
+  int B, C, Hq, Hkv, G, d, DV, dv_parts, q_tiles, nsplit, max_prefix, window, Tpad;
+  int kpre_paged;            // 1: prefix keys from the paged pool; 0: dense Kt
+  const int32_t* block_table;
+  int max_pages, page_tokens, num_pages;
+  const int32_t* prefix_len;
+  const float* vs_pre;       // non-null: scale each key's softmax weight (unit-RMS values)
+  const float* vs_tail;
+  float c_log2;              // scale * log2(e)
+  __nv_bfloat16* out;        // [B][C][Hq*d] (nsplit == 1)
+  float* lse;                // [B][C][Hq] or null (nsplit == 1)
+  float* part_o;             // [nsplit][B*Hkv][q_tiles*128][d] (nsplit > 1)
+  float* part_ml;            // [nsplit][B*Hkv][q_tiles*128][2]
+};
+struct AttnTcMaps {
+  CUtensorMap q, kpre, vpre, kx, vx;
+};
+size_t attention_tc_smem_bytes(int d);
+cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream);
+cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream);
 
 }  // namespace canvas

@@ -71,7 +71,9 @@ class AttnCase:
         return self.out.float().cpu().numpy().astype(np.float64)
 
 
-def oracle_attention(inp: wl.AttnInputs, rows=None, v_unit_rms=False, scale=1.0):
+def oracle_attention(inp: wl.AttnInputs, rows=None, v_unit_rms=False, scale=1.0, slack_eps=None):
+    """fp64 oracle on the same inputs; bf16 workloads use the bf16 storage
+    model.  With ``slack_eps`` (bf16 only) returns (out, lse, slack)."""
     from oracle import attention as oatt
     c = inp.cfg
     dt = c.dtype
@@ -80,7 +82,7 @@ def oracle_attention(inp: wl.AttnInputs, rows=None, v_unit_rms=False, scale=1.0)
                                  c.Hkv, c.d, inp.gamma_q.astype(np.float64), inp.gamma_k.astype(np.float64), c.eps,
                                  inp.freq.astype(np.float64), c.layer, f64(inp.cache_k, dt), f64(inp.cache_v, dt),
                                  inp.prefix_len, c.window, scale=scale, v_unit_rms=v_unit_rms, storage=storage,
-                                 rows=rows)
+                                 rows=rows, slack_eps=slack_eps if dt == "bf16" else None)
 
 
 def attn_errors(got: np.ndarray, want: np.ndarray):

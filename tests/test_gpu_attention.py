@@ -3,6 +3,18 @@
 Tolerances: bf16 calls -- max |err| <= 2e-2 and relative Frobenius error
 <= 5e-3 (the bar set for the attention output in bf16); fp32 calls -- 1e-4 /
 1e-5 (fp32 arithmetic against fp64).
+
+bf16 storage decisions.  The path stores q, the canvas keys / values and the
+global keys in bf16; the oracle rounds the same tensors at the same points.
+Where an exact value lies within the path's fp32 arithmetic error of a bf16
+rounding midpoint both neighbours are correct stored values, and the sharp
+softmax of these workloads can turn such a flip into an output change above
+2e-2.  For every output element the oracle bounds that change over all
+combinations of such flips (``slack``); an element passes when
+|err| <= 2e-2 + slack.  Elements with no ambiguous decision upstream have
+slack 0 and face the plain 2e-2 bar; the relative Frobenius bar has no slack.
+The ambiguity window SLACK_EPS covers the path's measured fp32 error before
+rounding (projection + norm + rotation).
 """
 import numpy as np
 import pytest
@@ -14,6 +26,11 @@ from canvas_harness import AttnCase, attn_errors, oracle_attention
 pytestmark = pytest.mark.gpu
 
 BF16_MAX, BF16_FRO = 2e-2, 5e-3
+# ambiguity window relative to |x| + |pair partner| + row rms: twice the largest
+# fp32 projection error measured on the workloads (4.1e-6 of the row rms)
+SLACK_EPS = 2.0 ** -17
+# at most this fraction of the elements may need slack at all
+MAX_FRAC_OVER = 1e-4
 FP32_MAX, FP32_FRO = 1e-4, 1e-5
 
 
@@ -36,16 +53,25 @@ def check(cv, cfg, rows=None, v_unit_rms=False, page_seed=1234):
     inp = wl.make_attention_inputs(cfg)
     case = AttnCase(inp, page_seed=page_seed).run(v_unit_rms=int(v_unit_rms))
     assert case.status() == cv.CANVAS_OK, cv.canvas_last_error()
-    want, want_lse = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms)
     got = case.out_f64()
-    mx, rf = attn_errors(got, want)
+    if cfg.dtype == "bf16":
+        want, want_lse, slack = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms, slack_eps=SLACK_EPS)
+        mx, rf = attn_errors(got, want)
+        m = np.isfinite(want)
+        err = np.abs(got - want)[m]
+        over = err > BF16_MAX
+        print(f"{cfg.name}: max|err| {mx:.4g}, rel-Fro {rf:.3g}, {int(over.sum())} of {err.size} elements above "
+              f"{BF16_MAX} (largest slack used {float(np.max(slack[m][over], initial=0.0)):.3g})")
+        assert rf <= BF16_FRO, rf
+        assert np.all(err <= BF16_MAX + slack[m]), float(np.max(err - BF16_MAX - slack[m]))
+        assert over.mean() <= MAX_FRAC_OVER, over.mean()
+    else:
+        want, want_lse = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms)
+        mx, rf = attn_errors(got, want)
+        assert mx <= FP32_MAX and rf <= FP32_FRO, (mx, rf)
     lse = case.lse.cpu().numpy().astype(np.float64)
     m = np.isfinite(want_lse)
     lse_err = float(np.max(np.abs(lse[m] - want_lse[m]) / (1.0 + np.abs(want_lse[m]))))
-    if cfg.dtype == "bf16":
-        assert mx <= BF16_MAX and rf <= BF16_FRO, (mx, rf)
-    else:
-        assert mx <= FP32_MAX and rf <= FP32_FRO, (mx, rf)
     assert lse_err < 1e-3, lse_err
     if rows is None:
         assert np.all(np.isfinite(got))
@@ -63,6 +89,7 @@ def test_tiny_fp32_workload(cv):
     small(prefix=(0, 64), C=33),                               # empty prefix / page-aligned prefix
     small(B=1, C=1, prefix=(70,), Hq=2, Hkv=1),                # one canvas token
     small(Hq=8, Hkv=1, d=256, D=512),                          # GQA 8:1, head_dim 256
+    small(d=64, prefix=(1000, 513), window=300, C=200),        # head_dim 64, several KV splits, 64-unaligned prefix
     small(layer="global", window=0, theta=1e6, rotary_fraction=0.25),
     small(layer="global", window=0, theta=1e6, rotary_fraction=0.25, Hq=8, Hkv=1, d=512, D=512,
           prefix=(200, 64), C=64),
