@@ -37,8 +37,11 @@ CANVAS_LAYER_GLOBAL = 1
 EXPORTED = [
     "canvas_attention_workspace_size", "canvas_attention", "canvas_sample_workspace_size", "canvas_sample",
     "canvas_gemm_workspace_size", "canvas_gemm_bf16", "canvas_last_error", "canvas_device_status",
-    "canvas_version", "canvas_profile_events", "canvas_kernel_launches",
+    "canvas_version", "canvas_profile_events", "canvas_kernel_launches", "canvas_gemm_bf16_noalloc",
 ]
+
+# size of the static scratch behind canvas_gemm_bf16_noalloc (include/canvas.h)
+CANVAS_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 CANVAS_KERNEL_ATTENTION = 0
 CANVAS_KERNEL_PREP = 1
@@ -77,6 +80,8 @@ def _load():
     lib.canvas_gemm_workspace_size.restype = Z
     lib.canvas_gemm_bf16.argtypes = [P, P, I, P, I, I, I, I, P, Z, P]
     lib.canvas_gemm_bf16.restype = I
+    lib.canvas_gemm_bf16_noalloc.argtypes = [P, P, I, P, I, I, I, I, P]
+    lib.canvas_gemm_bf16_noalloc.restype = I
     lib.canvas_last_error.argtypes = []
     lib.canvas_last_error.restype = ctypes.c_char_p
     lib.canvas_device_status.argtypes = [P]
@@ -190,6 +195,14 @@ def canvas_gemm_bf16(A, B, b_layout, C, accumulate, workspace, stream=None):
     N = B.shape[0] if b_layout == 0 else B.shape[1]
     _check(lib.canvas_gemm_bf16(_ptr(A), _ptr(B), int(b_layout), _ptr(C), M, N, K, int(accumulate),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def canvas_gemm_bf16_noalloc(A, B, b_layout, C, accumulate, stream=None):
+    """canvas_gemm_bf16 with the library's static scratch instead of a workspace."""
+    M, K = A.shape
+    N = B.shape[0] if b_layout == 0 else B.shape[1]
+    _check(lib.canvas_gemm_bf16_noalloc(_ptr(A), _ptr(B), int(b_layout), _ptr(C), M, N, K, int(accumulate),
+                                        _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

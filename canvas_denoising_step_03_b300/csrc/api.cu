@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -308,6 +309,47 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
   if (!ws_ok(workspace, ws_bytes, canvas_gemm_workspace_size(M, N, K)))
     return fail(CANVAS_ERR_WORKSPACE, "canvas_gemm_bf16: workspace missing, small or misaligned");
   return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ GEMM without a workspace
+// The split-K scratch of canvas_gemm_bf16_noalloc: one static device array,
+// shared by every call on a device.  Host code cannot use the symbol as a
+// pointer; its device address is looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CANVAS_GEMM_NOALLOC_SCRATCH_BYTES];
+
+canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layout, float* C, int M, int N, int K,
+                                       int accumulate, canvas_stream_t stream) {
+  if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: null pointer");
+  if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: bad shape");
+  if (b_layout != 0 && b_layout != 1)
+    return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: b_layout must be 0 or 1");
+  if (K % 8 != 0 || N % 8 != 0)
+    return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16_noalloc: K and N must be multiples of 8");
+  const size_t need = canvas_gemm_workspace_size(M, N, K);
+  if (need > CANVAS_GEMM_NOALLOC_SCRATCH_BYTES)
+    return fail(CANVAS_ERR_WORKSPACE,
+                "canvas_gemm_bf16_noalloc: this shape needs %zu bytes of scratch, the static scratch holds %u "
+                "(use canvas_gemm_bf16 with a workspace)",
+                need, CANVAS_GEMM_NOALLOC_SCRATCH_BYTES);
+  // device address of the static scratch, looked up once per device
+  constexpr int kMaxDevices = 64;
+  static void* scratch[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  CANVAS_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16_noalloc: device id");
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (scratch[dev] == nullptr) {
+      void* p = nullptr;
+      CANVAS_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+      scratch[dev] = p;
+    }
+    ws = scratch[dev];
+  }
+  // run_gemm_tc zeroes the split-K tickets it uses before every launch
+  return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int max_prefix,

@@ -218,6 +218,34 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
                                void* workspace, size_t ws_bytes, canvas_stream_t stream);
 
 /*
+ * canvas_gemm_bf16_noalloc -- canvas_gemm_bf16 without a caller workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot hand the library a device buffer: code running inside a host
+ * application whose allocator owns every byte of device memory and forbids
+ * raw cudaMalloc, or that must not allocate after start-up (a fixed memory
+ * budget, or a latency-critical path where an allocation could synchronise
+ * the device).
+ *
+ * Same operation, arguments, layouts and result as canvas_gemm_bf16.  The
+ * split-K scratch lives in one static device array of
+ * CANVAS_GEMM_NOALLOC_SCRATCH_BYTES bytes inside the library; every device
+ * that loads the library holds it until the process exits.  Shapes whose
+ * scratch (canvas_gemm_workspace_size) exceeds that size return
+ * CANVAS_ERR_WORKSPACE with a message.  No call allocates or frees device
+ * memory.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array: calls that may overlap on the GPU (different
+ * streams, or different host threads, without ordering between them) race
+ * on it and must be serialised by the caller.
+ */
+#define CANVAS_GEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layout, float* C,
+                                       int M, int N, int K, int accumulate, canvas_stream_t stream);
+
+/*
  * Kernel timing hooks, for benchmarks.  When a pair of events is registered
  * for a kernel id, every later call on this thread records `start` on the
  * call's stream immediately before that kernel's launch and `stop` right
