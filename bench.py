@@ -21,7 +21,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -75,53 +74,107 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """SM clock, power and clock-event (throttle) reasons sampled through NVML
+    every few milliseconds on a background thread during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown", 0x8),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap", 0x4))
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = f"/tmp/canvas_clocks_{os.getpid()}.csv"
+    def __init__(self, gpu_index: int, period_s: float = 0.004):
+        self.gpu, self.period = gpu_index, period_s
+        self.samples, self.thread, self.nv = [], None, None
 
     def start(self):
+        import threading
         try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
-                                         stderr=subprocess.DEVNULL)
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            self.h = nv.nvmlDeviceGetHandleByIndex(self.gpu)
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+        except Exception as e:  # no NVML binding: sample through nvidia-smi instead
+            self.err = repr(e)
+            self._start_smi()
+            return
+        self.stop_flag = threading.Event()
+
+        def loop():
+            nv = self.nv
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            while not self.stop_flag.is_set():
+                try:
+                    self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
+                                         nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0, int(get_reasons(self.h))))
+                except Exception:
+                    pass
+                self.stop_flag.wait(self.period)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.hw_power_brake_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def _start_smi(self):
+        import subprocess
+        import tempfile
+        self.smi_file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.smi = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.SMI_FIELDS}",
+                                         "--format=csv,noheader,nounits", "-lms", "10"], stdout=self.smi_file,
+                                        stderr=subprocess.DEVNULL)
+        except Exception as e:
+            self.smi, self.err = None, self.err + "; " + repr(e)
+
+    def _stop_smi(self):
+        self.smi.terminate()
+        try:
+            self.smi.wait(timeout=5)
         except Exception:
-            self.proc = None
+            self.smi.kill()
+        self.smi_file.seek(0)
+        sm, mx, pw, reasons = [], [], [], set()
+        for line in self.smi_file:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for (name, _, _), v in zip(self.REASONS, parts[3:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        self.smi_file.close()
+        os.unlink(self.smi_file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw) if pw else None,
+                "source": "nvidia-smi -lms 10"}
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(nm)
-        os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self.thread is None:
+            if getattr(self, "smi", None) is not None:
+                return self._stop_smi()
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no clock source: {getattr(self, 'err', '')}"]}
+        self.stop_flag.set()
+        self.thread.join()
+        reasons = set()
+        for _, _, bits in self.samples:
+            for name, const, default in self.REASONS:
+                if bits & getattr(self.nv, const, default):
+                    reasons.add(name)
+        sm = [c for c, _, _ in self.samples]
+        pw = [w for _, w, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": round(max(pw), 1) if pw else None, "source": "nvml"}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -423,7 +476,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

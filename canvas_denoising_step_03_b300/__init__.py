@@ -61,10 +61,10 @@ class canvas_kv_cache(ctypes.Structure):
                 ("num_pages", ctypes.c_int32)]
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libcanvas.so not built ({LIB_PATH}); run __graft_entry__.build()")
-    lib = ctypes.CDLL(LIB_PATH)
+def _load(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"libcanvas.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
     P, I, F, Z, U64, U32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64,
                             ctypes.c_uint32)
     lib.canvas_attention_workspace_size.argtypes = [I] * 9

@@ -119,7 +119,7 @@ canvas_status make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, ui
 // ------------------------------------------------------------------ GEMM plan
 struct GemmPlan {
   int m_tiles, n_tiles, kblocks, splits, two_acc;
-  size_t partial_bytes, counter_bytes;
+  size_t partial_bytes;
 };
 
 constexpr int kNumSms = 148;
@@ -135,13 +135,12 @@ GemmPlan plan_gemm(int M, int N, int K) {
   s = std::min(s, std::max(1, p.kblocks / 2));
   p.splits = std::max(1, s);
   p.partial_bytes = p.splits > 1 ? size_t(p.splits) * M * N * sizeof(float) : 0;
-  p.counter_bytes = size_t(tiles) * sizeof(int);
   return p;
 }
 
-size_t gemm_ws_bytes(const GemmPlan& p) { return align_up(p.partial_bytes) + align_up(p.counter_bytes); }
+size_t gemm_ws_bytes(const GemmPlan& p) { return align_up(p.partial_bytes); }
 
-// C[M,N] = A[M,K] op(B) on the tensor cores; ws holds partials + counters.
+// C[M,N] = A[M,K] op(B) on the tensor cores; ws holds the split partials.
 canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C, int M, int N, int K,
                           int accumulate, void* ws, cudaStream_t stream) {
   const GemmPlan p = plan_gemm(M, N, K);
@@ -156,7 +155,6 @@ canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C
   Carver cv(ws);
   GemmTcArgs g;
   g.partials = cv.take<float>(p.partial_bytes);
-  g.counters = cv.take<int>(p.counter_bytes);
   g.C = C;
   g.M = M;
   g.N = N;
@@ -169,7 +167,6 @@ canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C
   g.n_tiles = p.n_tiles;
   g.splits = p.splits;
   g.kblocks = p.kblocks;
-  if (p.splits > 1) CANVAS_CUDA(cudaMemsetAsync(g.counters, 0, p.counter_bytes, stream));
   CANVAS_CUDA(launch_gemm_tc(tmA, tmB, g, stream));
   return CANVAS_OK;
 }
@@ -348,7 +345,7 @@ canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layou
     }
     ws = scratch[dev];
   }
-  // run_gemm_tc zeroes the split-K tickets it uses before every launch
+  // the scratch holds only split partials, fully rewritten by every call
   return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -373,6 +370,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   if (global && W_v != nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: global layers share W_v = W_k (pass NULL)");
   if (!global && W_v == nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: sliding layers need W_v");
   if (v_unit_rms && !global) return fail(CANVAS_ERR_ARG, "canvas_attention: v_unit_rms applies to global layers");
+  if (!(scale > 0.f)) return fail(CANVAS_ERR_ARG, "canvas_attention: scale must be > 0");
   if (max_prefix > 0 && (!kv->k_pool || !kv->block_table)) return fail(CANVAS_ERR_ARG, "canvas_attention: cache pointers");
   if (max_prefix > 0 && !global && !kv->v_pool) return fail(CANVAS_ERR_ARG, "canvas_attention: sliding cache needs v_pool");
   if (global && kv->v_pool) return fail(CANVAS_ERR_ARG, "canvas_attention: global cache has no v_pool");
@@ -582,6 +580,8 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
   if (probs_out && probs_dtype != CANVAS_BF16 && probs_dtype != CANVAS_FP32)
     return fail(CANVAS_ERR_ARG, "canvas_sample: probs_dtype");
   if (V % 8 != 0 || D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_sample: V and D must be multiples of 8");
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs_out)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_sample: logits and probs_out must be 16-byte aligned");
   const SampleLayout L = sample_layout(dtype, rows, V, D);
   if (!ws_ok(workspace, ws_bytes, L.total))
     return fail(CANVAS_ERR_WORKSPACE, "canvas_sample: workspace missing, small or misaligned (need %zu)", L.total);

@@ -55,7 +55,7 @@ struct Cfg {
   static constexpr int NCH = D / 64;             // 64-wide chunks of the head dimension
   static constexpr int KCH = NCH < 2 ? NCH : 2;  // chunks per K stage
   static constexpr int KST = NCH / KCH;          // K stages per block
-  static constexpr int NST = D == 512 ? 3 : 4;   // ring stages
+  static constexpr int NST = D == 512 ? 3 : 5;   // ring stages
   static constexpr int QBytes = NCH * 16384;
   static constexpr int Smem = QBytes + NST * kStageBytes + 1024 + 256;
 };
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&s_full[j], 1);
-      mbar_init(&p_full[j], 128);
+      mbar_init(&p_full[j], 4);  // one arrival per softmax warp
       mbar_init(&pv_done[j], 1);
     }
     mbar_init(drain, 1);
@@ -344,42 +344,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           clean = clean && (t0 + 64 <= sq.T) && (sq.P64 + t0 >= sq.lo_max || sq.P64 + t0 >= sq.P);
         }
       }
-      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      // S row of this thread: 128 fp32 values in registers (four TMEM loads in flight)
+      uint32_t sv[kAttnBN];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c4 * 32]));
+      tmem_ld_wait();
       if (!clean) {
-        for (int c = 0; c < kAttnBN; ++c) {
-          const int sb = 2 * kb + (c >> 6), off = c & 63;
-          bool v;
+        // within sub-block u the visible keys are the offsets [lo_off, hi_off):
+        // position >= the row's window start (lo_row <= P, so canvas keys pass)
+        // and, in the tail, rows before the zero padding
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int sb = 2 * kb + u;
+          int pos0, hi_off = 64;
           if (sb < sq.n_pre) {
-            v = sq.s0 + 64 * sb + off >= lo_row;
+            pos0 = sq.s0 + 64 * sb;
           } else {
-            const int t = 64 * (sb - sq.n_pre) + off;
-            const int pos = sq.P64 + t;
-            v = (t < sq.T) && (pos >= sq.P || pos >= lo_row);
+            const int t0 = 64 * (sb - sq.n_pre);
+            pos0 = sq.P64 + t0;
+            hi_off = min(64, sq.T - t0);
           }
-          if (!v) vis[c >> 5] &= ~(1u << (c & 31));
+          const int lo_off = max(0, lo_row - pos0);
+#pragma unroll
+          for (int off = 0; off < 64; ++off)
+            if (off < lo_off || off >= hi_off) sv[u * 64 + off] = __float_as_uint(-INFINITY);
         }
       }
-      // pass 1: block maximum (log2 domain)
-      float bmax = -INFINITY;
+      // block maximum in the log2 domain (c_log2 > 0)
+      float smax = __uint_as_float(sv[0]);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(tS + c4 * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((vis[c4] >> j) & 1u) bmax = fmaxf(bmax, __uint_as_float(r[j]) * a.c_log2);
-      }
+      for (int c = 1; c < kAttnBN; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
+      const float bmax = smax * a.c_log2;
       const float m_new = fmaxf(m_run, bmax);
       const bool need = (m_run != -INFINITY) && (m_new > m_run + kRescaleLog2);
+      const float alpha = need ? exp2f(m_run - m_new) : 1.f;
+      if (need) {
+        l *= alpha;
+        m_run = m_new;
+      } else if (m_run == -INFINITY) {
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // P = 2^(s c - m) rounded to bf16 pairs, written over the first 64 columns
+      // of S (keys 32 c4 .. 32 c4 + 31 -> columns 16 c4 .. 16 c4 + 15; the S
+      // values are already in registers)
+      float l_lo = 0.f, l_hi = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c4 * 32 + 2 * j;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), a.c_log2, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), a.c_log2, -m_use));
+          if (a.vs_pre == nullptr) {
+            pk[j] = pack_bf16x2(p0, p1);
+            // the sum uses the rounded weights, so O / l is an exact convex
+            // combination of value rows with the stored weights
+            l_lo += __uint_as_float(pk[j] << 16);
+            l_hi += __uint_as_float(pk[j] & 0xffff0000u);
+          } else {
+            // unit-RMS values: weight of each key times its row scalar sc; the
+            // sum divides the stored product back by sc for the same reason
+            float sc[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ce = c + e, sb = 2 * kb + (ce >> 6), off = ce & 63;
+              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + sq.s0 + 64 * sb + off]
+                                    : a.vs_tail[(size_t)grp * a.Tpad + 64 * (sb - sq.n_pre) + off];
+            }
+            pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
+            const float w0 = __uint_as_float(pk[j] << 16), w1 = __uint_as_float(pk[j] & 0xffff0000u);
+            l_lo += sc[0] > 0.f ? w0 / sc[0] : 0.f;
+            l_hi += sc[1] > 0.f ? w1 / sc[1] : 0.f;
+          }
+        }
+        tmem_st16(tS + c4 * 16, pk);
+      }
+      l += l_lo + l_hi;
+      // rescale O (after P is stored, so the S registers are free): the
+      // previous block's P.V must have landed in O first; P.V of this block
+      // waits for the arrival below
       if (__any_sync(0xffffffffu, need)) {
-        // the previous block's P.V must have landed in O before it is rescaled
         if (!mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        const float alpha = need ? exp2f(m_run - m_new) : 1.f;
 #pragma unroll 1
         for (int cc = 0; cc < K::DV / 32; ++cc) {
           uint32_t r[32];
@@ -389,54 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
           tmem_st32(tmem + lane_off + cc * 32, r);
         }
-        tmem_st_wait();
-      }
-      if (need) {
-        l *= exp2f(m_run - m_new);
-        m_run = m_new;
-      } else if (m_run == -INFINITY) {
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(s c - m) rounded to bf16 pairs, written over the first
-      // 64 columns of S (keys 32 c4 .. 32 c4 + 31 -> columns 16 c4 .. 16 c4 + 15;
-      // those S columns were read in this or an earlier chunk)
-#pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[32], pk[16];
-        tmem_ld32(tS + c4 * 32, r);
-        tmem_ld_wait();
-        const uint32_t vw = vis[c4];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float x0 = ((vw >> (2 * j)) & 1u) ? __uint_as_float(r[2 * j]) * a.c_log2 - m_use : -INFINITY;
-          const float x1 = ((vw >> (2 * j + 1)) & 1u) ? __uint_as_float(r[2 * j + 1]) * a.c_log2 - m_use : -INFINITY;
-          const float p0 = exp2f(x0), p1 = exp2f(x1);
-          if (a.vs_pre == nullptr) {
-            pk[j] = pack_bf16x2(p0, p1);
-            // the sum uses the rounded weights, so O / l is an exact convex
-            // combination of value rows with the stored weights
-            l += bf16_bits_to_f32(pk[j] & 0xffffu) + bf16_bits_to_f32(pk[j] >> 16);
-          } else {
-            // unit-RMS values: weight of each key times its row scalar sc; the
-            // sum divides the stored product back by sc for the same reason
-            float sc[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int ce = c4 * 32 + 2 * j + e, sb = 2 * kb + (ce >> 6), off = ce & 63;
-              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + sq.s0 + 64 * sb + off]
-                                    : a.vs_tail[(size_t)grp * a.Tpad + 64 * (sb - sq.n_pre) + off];
-            }
-            pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
-            const float w0 = bf16_bits_to_f32(pk[j] & 0xffffu), w1 = bf16_bits_to_f32(pk[j] >> 16);
-            l += (sc[0] > 0.f ? w0 / sc[0] : 0.f) + (sc[1] > 0.f ? w1 / sc[1] : 0.f);
-          }
-        }
-        tmem_st16(tS + c4 * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[n & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[n & 1]);
     }
     if (alive && nb >= 1) {
       alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);

@@ -17,12 +17,15 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulators (each warp reads the
 //               32 TMEM lanes of its quadrant) and fp32 stores.
 // K is split across CTAs when the tile grid alone cannot fill the 148 SMs;
-// partial tiles go to a workspace and the last CTA of a tile (atomic ticket)
-// sums them in split order, so the result does not depend on timing.
+// each split writes its fp32 partial tile to the workspace and a separate
+// reduce kernel sums the splits in order (so the result does not depend on
+// timing), spread over the whole GPU.
 // Every mbarrier wait is bounded (common.cuh): on timeout the CTA records
 // CANVAS_ERR_TIMEOUT, drains and returns.
 #include "common.cuh"
 #include "kernels.h"
+
+#include <algorithm>
 
 namespace canvas {
 
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kGemmStages;
   uint64_t* tmem_full = empty + kGemmStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort, [1] last-CTA
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x, mt = blockIdx.y, split = blockIdx.z;
@@ -64,7 +67,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tmem_full, 1);
     flags[0] = 0;
-    flags[1] = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -180,43 +182,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (ok && g.splits > 1) {
-      // ticket: the last CTA of this tile sums the partials in split order
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 2 && lane == 0) {
-        const int t = atomicAdd(&g.counters[mt * g.n_tiles + nt], 1);
-        flags[1] = (t == g.splits - 1) ? 1 : 0;
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (flags[1]) {
-        __threadfence();
-        const int rows_here = nacc * 128;
-        const int col_lo = nt * kGemmBN, col_hi = min(g.N, col_lo + kGemmBN);
-        // 128 threads: each walks rows, columns in float4 steps
-        const int et = (warp - 2) * 32 + lane;
-        for (int rr = 0; rr < rows_here; ++rr) {
-          const int row = mt * 256 + rr;
-          if (row >= g.M) break;
-          for (int c = col_lo + et * 4; c < col_hi; c += 128 * 4) {
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (g.accumulate) s4 = *reinterpret_cast<const float4*>(g.C + (size_t)row * g.ldc + c);
-            for (int sp = 0; sp < g.splits; ++sp) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(g.partials + ((size_t)sp * g.M + row) * g.N + c));
-              s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
-            }
-            *reinterpret_cast<float4*>(g.C + (size_t)row * g.ldc + c) = s4;
-          }
-        }
-        if (warp == 2 && lane == 0) g.counters[mt * g.n_tiles + nt] = 0;
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// C[m][n] = (accumulate ? C : 0) + sum over splits s (in order) of partials[s][m][n]
+__global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float4* __restrict__ partials, float4* C,
+                                                                 long long n4, int splits, int accumulate) {
+  for (long long e = blockIdx.x * 256LL + threadIdx.x; e < n4; e += (long long)gridDim.x * 256) {
+    float4 s4 = accumulate ? C[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < splits; ++sp) {
+      const float4 v = __ldcs(partials + sp * n4 + e);
+      s4.x += v.x;
+      s4.y += v.y;
+      s4.z += v.z;
+      s4.w += v.w;
+    }
+    C[e] = s4;
   }
 }
 
@@ -231,6 +218,13 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   }
   dim3 grid(g.n_tiles, g.m_tiles, g.splits);
   gemm_bf16_tc_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, g);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || g.splits == 1) return e;
+  const long long n4 = (long long)g.M * g.N / 4;  // N % 8 == 0
+  const int blocks = int(std::min<long long>((n4 + 255) / 256, 148LL * 8));
+  gemm_split_reduce_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(g.partials),
+                                                       reinterpret_cast<float4*>(g.C), n4, g.splits, g.accumulate);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -43,8 +43,7 @@ struct GemmTcArgs {
   int b_mn_major;  // 0: B is [N,K] (K contiguous); 1: B is [K,N] (N contiguous)
   int two_acc;     // 1: a CTA covers 256 rows (two 128-row accumulators)
   int m_tiles, n_tiles, splits, kblocks;
-  float* partials;  // [splits][M][N] when splits > 1
-  int* counters;    // [m_tiles * n_tiles], zero before the launch
+  float* partials;  // [splits][M][N] when splits > 1 (ldc == N), summed by a reduce kernel
 };
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 3;
 size_t gemm_tc_smem_bytes();

@@ -50,59 +50,114 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 constexpr int kMaxPairsPerLane = 8;  // d <= 512: d/2 / 32 pairs per lane
 
-// One row held by a warp as pairs (lo[k], hi[k]) = (x[t], x[t + d/2]),
-// t = lane + 32 k, k < np = d / 64.
+// One row held by a warp as pairs (lo[k], hi[k]) = (x[t], x[t + d/2]).  Lane
+// `lane` owns chunks c < kChunks of kVec consecutive elements,
+// t = (lane + 32 c) * kVec + e: each warp access covers 32 * kVec contiguous
+// elements (coalesced), and the rotated pairs of a partial RoPE (the leading
+// frequencies) are spread over all lanes rather than packed into a few.
 struct Row {
   float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
 };
 
-template <typename T>
-__device__ __forceinline__ void load_row(const T* src, int d, Row& r) {
-  const int lane = threadIdx.x & 31, half = d / 2, np = half / 32;
-#pragma unroll
-  for (int k = 0; k < kMaxPairsPerLane; ++k) {
-    if (k < np) {
-      r.lo[k] = to_f32(src[lane + 32 * k]);
-      r.hi[k] = to_f32(src[half + lane + 32 * k]);
+template <int D>
+struct RowShape {
+  static constexpr int half = D / 2;
+  static constexpr int np = half / 32;                 // elements per lane per half
+  static constexpr int kVec = (np % 2 == 0) ? 2 : 1;   // consecutive elements per access
+  static constexpr int kChunks = np / kVec;
+  __device__ __forceinline__ static int elem(int lane, int k) { return (lane + 32 * (k / kVec)) * kVec + k % kVec; }
+};
+
+template <typename T, int N>
+struct VecIO;
+template <int N>
+struct VecIO<__nv_bfloat16, N> {
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* x) {
+    if constexpr (N == 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+      x[0] = __uint_as_float(u << 16);
+      x[1] = __uint_as_float(u & 0xffff0000u);
+    } else {
+      x[0] = __bfloat162float(p[0]);
     }
+  }
+  __device__ __forceinline__ static void store(__nv_bfloat16* p, const float* x) {
+    if constexpr (N == 2)
+      *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(x[0], x[1]);
+    else
+      p[0] = __float2bfloat16_rn(x[0]);
+  }
+};
+template <int N>
+struct VecIO<float, N> {
+  __device__ __forceinline__ static void load(const float* p, float* x) {
+    if constexpr (N == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(p);
+      x[0] = v.x;
+      x[1] = v.y;
+    } else {
+      x[0] = p[0];
+    }
+  }
+  __device__ __forceinline__ static void store(float* p, const float* x) {
+    if constexpr (N == 2)
+      *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    else
+      p[0] = x[0];
+  }
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void load_row(const T* src, Row& r) {
+  using S = RowShape<D>;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < S::kChunks; ++c) {
+    const int t = (lane + 32 * c) * S::kVec;
+    VecIO<T, S::kVec>::load(src + t, r.lo + c * S::kVec);
+    VecIO<T, S::kVec>::load(src + S::half + t, r.hi + c * S::kVec);
   }
 }
 
-__device__ __forceinline__ float row_norm(const Row& r, int d) {
-  const int np = d / 64;
+template <typename T, int D>
+__device__ __forceinline__ void store_row(T* dst, const Row& r) {
+  using S = RowShape<D>;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < S::kChunks; ++c) {
+    const int t = (lane + 32 * c) * S::kVec;
+    VecIO<T, S::kVec>::store(dst + t, r.lo + c * S::kVec);
+    VecIO<T, S::kVec>::store(dst + S::half + t, r.hi + c * S::kVec);
+  }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void zero_row(T* dst) {
+  Row z;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerLane; ++k) z.lo[k] = z.hi[k] = 0.f;
+  store_row<T, D>(dst, z);
+}
+
+template <int D>
+__device__ __forceinline__ float row_norm(const Row& r) {
+  constexpr int np = D / 64;
   float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < kMaxPairsPerLane; ++k)
-    if (k < np) ss += r.lo[k] * r.lo[k] + r.hi[k] * r.hi[k];
+  for (int k = 0; k < np; ++k) ss += r.lo[k] * r.lo[k] + r.hi[k] * r.hi[k];
   return sqrtf(warp_sum(ss));
 }
 
-template <typename T>
-__device__ __forceinline__ void store_row(T* dst, int d, const Row& r) {
-  const int lane = threadIdx.x & 31, half = d / 2, np = half / 32;
-#pragma unroll
-  for (int k = 0; k < kMaxPairsPerLane; ++k) {
-    if (k < np) {
-      dst[lane + 32 * k] = from_f32<T>(r.lo[k]);
-      dst[half + lane + 32 * k] = from_f32<T>(r.hi[k]);
-    }
-  }
-}
-
-template <typename T>
-__device__ __forceinline__ void zero_row(T* dst, int d) {
-  for (int t = threadIdx.x & 31; t < d; t += 32) dst[t] = from_f32<T>(0.f);
-}
-
 // rotate(rms(x, gamma)) at position pos, in place (fp32)
-__device__ __forceinline__ void norm_rope(Row& r, int d, const float* gamma, float eps, const float* freq,
-                                          int pos) {
-  const int lane = threadIdx.x & 31, half = d / 2, np = half / 32;
-  const float scale = sqrtf(float(d)) / (row_norm(r, d) + eps);
+template <int D>
+__device__ __forceinline__ void norm_rope(Row& r, const float* gamma, float eps, const float* freq, int pos) {
+  using S = RowShape<D>;
+  constexpr int np = S::np, half = S::half;
+  const int lane = threadIdx.x & 31;
+  const float scale = sqrtf(float(D)) / (row_norm<D>(r) + eps);
 #pragma unroll
-  for (int k = 0; k < kMaxPairsPerLane; ++k) {
-    if (k >= np) break;
-    const int t = lane + 32 * k;
+  for (int k = 0; k < np; ++k) {
+    const int t = S::elem(lane, k);
     const float a = gamma[t] * r.lo[k] * scale;
     const float b = gamma[t + half] * r.hi[k] * scale;
     const float f = freq[t];
@@ -118,34 +173,31 @@ __device__ __forceinline__ void norm_rope(Row& r, int d, const float* gamma, flo
   }
 }
 
-template <typename T>
-__device__ __forceinline__ void round_row(Row& r, int d) {
-  const int np = d / 64;
+template <typename T, int D>
+__device__ __forceinline__ void round_row(Row& r) {
 #pragma unroll
-  for (int k = 0; k < kMaxPairsPerLane; ++k) {
-    if (k < np) {
-      r.lo[k] = stored<T>(r.lo[k]);
-      r.hi[k] = stored<T>(r.hi[k]);
-    }
+  for (int k = 0; k < D / 64; ++k) {
+    r.lo[k] = stored<T>(r.lo[k]);
+    r.hi[k] = stored<T>(r.hi[k]);
   }
 }
 
 // Global layers: from a stored raw row r at position pos, write the key
 // rotate(rms(r)) to kdst, r itself to vdst (if non-null) and the value row
 // scalar sqrt(d) / (|r| + eps) to *vs (lane 0).
-template <typename T>
-__device__ __forceinline__ void global_row(Row& r, int d, const float* gamma_k, float eps, const float* freq,
-                                           int pos, T* kdst, T* vdst, float* vs) {
-  if (vdst) store_row(vdst, d, r);
-  const float nrm = row_norm(r, d);
-  if (vs && (threadIdx.x & 31) == 0) *vs = sqrtf(float(d)) / (nrm + eps);
-  norm_rope(r, d, gamma_k, eps, freq, pos);
-  store_row(kdst, d, r);
+template <typename T, int D>
+__device__ __forceinline__ void global_row(Row& r, const float* gamma_k, float eps, const float* freq, int pos,
+                                           T* kdst, T* vdst, float* vs) {
+  if (vdst) store_row<T, D>(vdst, r);
+  const float nrm = row_norm<D>(r);
+  if (vs && (threadIdx.x & 31) == 0) *vs = sqrtf(float(D)) / (nrm + eps);
+  norm_rope<D>(r, gamma_k, eps, freq, pos);
+  store_row<T, D>(kdst, r);
 }
 
 // One warp per (canvas token, head).  Heads: Hq query heads, then Hkv key
 // heads, then (sliding) Hkv value heads.
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int G = p.Hq / p.Hkv;
@@ -155,7 +207,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
   const int row = warp_global / heads;  // token b*C + i
   const int hh = warp_global % heads;
   const int b = row / p.C, i = row % p.C;
-  const int d = p.d;
+  constexpr int d = D;
   const int P = p.prefix_len[b];
   if (P < 0) return;                     // reported by the key-prep kernel
   const int pos = P + i;
@@ -164,26 +216,26 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
   Row r;
   if (hh < p.Hq) {
     const int h = hh, hk = h / G, g = h % G;
-    load_row(p.proj_q + (size_t)row * p.Hq * d + (size_t)h * d, d, r);
-    norm_rope(r, d, p.gamma_q, p.eps, p.freq, pos);
-    store_row(static_cast<T*>(p.Qp) + ((((size_t)b * p.Hkv + hk) * G + g) * p.C + i) * d, d, r);
+    load_row<float, D>(p.proj_q + (size_t)row * p.Hq * d + (size_t)h * d, r);
+    norm_rope<D>(r, p.gamma_q, p.eps, p.freq, pos);
+    store_row<T, D>(static_cast<T*>(p.Qp) + ((((size_t)b * p.Hkv + hk) * G + g) * p.C + i) * d, r);
   } else if (hh < p.Hq + p.Hkv) {
     const int hk = hh - p.Hq;
-    load_row(p.proj_k + (size_t)row * p.Hkv * d + (size_t)hk * d, d, r);
+    load_row<float, D>(p.proj_k + (size_t)row * p.Hkv * d + (size_t)hk * d, r);
     const size_t trow = ((size_t)b * p.Hkv + hk) * p.Tpad + t;
     T* kdst = static_cast<T*>(p.Kx) + trow * d;
     if (p.global) {
-      round_row<T>(r, d);  // the stored raw row r: value, and source of the key
-      global_row<T>(r, d, p.gamma_k, p.eps, p.freq, pos, kdst, static_cast<T*>(p.Vx) + trow * d,
-                    p.vs_tail + trow);
+      round_row<T, D>(r);  // the stored raw row r: value, and source of the key
+      global_row<T, D>(r, p.gamma_k, p.eps, p.freq, pos, kdst, static_cast<T*>(p.Vx) + trow * d,
+                       p.vs_tail + trow);
     } else {
-      norm_rope(r, d, p.gamma_k, p.eps, p.freq, pos);
-      store_row(kdst, d, r);
+      norm_rope<D>(r, p.gamma_k, p.eps, p.freq, pos);
+      store_row<T, D>(kdst, r);
     }
   } else {
     const int hk = hh - p.Hq - p.Hkv;
-    load_row(p.proj_v + (size_t)row * p.Hkv * d + (size_t)hk * d, d, r);
-    store_row(static_cast<T*>(p.Vx) + (((size_t)b * p.Hkv + hk) * p.Tpad + t) * d, d, r);
+    load_row<float, D>(p.proj_v + (size_t)row * p.Hkv * d + (size_t)hk * d, r);
+    store_row<T, D>(static_cast<T*>(p.Vx) + (((size_t)b * p.Hkv + hk) * p.Tpad + t) * d, r);
   }
 }
 
@@ -192,7 +244,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
 // [max_prefix, max_prefix + Tpad): tail row t = row - max_prefix -- prefix
 // rows P64 + t < P are gathered from the cache, rows past the canvas are
 // zeroed, canvas rows are left to the prologue kernel.
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -209,7 +261,7 @@ __global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
     return;
   }
   const int P64 = P & ~63;
-  const int d = k.d;
+  constexpr int d = D;
   int pos, t = -1;
   if (row < k.max_prefix) {
     pos = row;
@@ -219,8 +271,8 @@ __global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
     pos = P64 + t;
     const size_t trow = ((size_t)b * k.Hkv + hk) * k.Tpad + t;
     if (pos >= P + k.C) {  // past the canvas: zero rows (finite operands for padded blocks)
-      zero_row(static_cast<T*>(k.Kx) + trow * d, d);
-      zero_row(static_cast<T*>(k.Vx) + trow * d, d);
+      zero_row<T, D>(static_cast<T*>(k.Kx) + trow * d);
+      zero_row<T, D>(static_cast<T*>(k.Vx) + trow * d);
       if (k.global && lane == 0) k.vs_tail[trow] = 0.f;
       return;
     }
@@ -235,23 +287,57 @@ __global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
   }
   const size_t src = (((size_t)page * k.Hkv + hk) * k.page_tokens + off) * d;
   Row r;
-  load_row(static_cast<const T*>(k.k_pool) + src, d, r);
+  load_row<T, D>(static_cast<const T*>(k.k_pool) + src, r);
   if (t < 0) {
     const size_t orow = ((size_t)b * k.Hkv + hk) * k.max_prefix + pos;
-    global_row<T>(r, d, k.gamma_k, k.eps, k.freq, pos, static_cast<T*>(k.Kt) + orow * d, nullptr,
-                  k.vs_pre + orow);
+    global_row<T, D>(r, k.gamma_k, k.eps, k.freq, pos, static_cast<T*>(k.Kt) + orow * d, nullptr,
+                     k.vs_pre + orow);
     return;
   }
   const size_t trow = ((size_t)b * k.Hkv + hk) * k.Tpad + t;
   if (k.global) {
-    global_row<T>(r, d, k.gamma_k, k.eps, k.freq, pos, static_cast<T*>(k.Kx) + trow * d,
-                  static_cast<T*>(k.Vx) + trow * d, k.vs_tail + trow);
+    global_row<T, D>(r, k.gamma_k, k.eps, k.freq, pos, static_cast<T*>(k.Kx) + trow * d,
+                     static_cast<T*>(k.Vx) + trow * d, k.vs_tail + trow);
   } else {
-    store_row(static_cast<T*>(k.Kx) + trow * d, d, r);
+    store_row<T, D>(static_cast<T*>(k.Kx) + trow * d, r);
     Row v;
-    load_row(static_cast<const T*>(k.v_pool) + src, d, v);
-    store_row(static_cast<T*>(k.Vx) + trow * d, d, v);
+    load_row<T, D>(static_cast<const T*>(k.v_pool) + src, v);
+    store_row<T, D>(static_cast<T*>(k.Vx) + trow * d, v);
   }
+}
+
+template <typename T>
+cudaError_t launch_prologue_t(const PrologueArgs& p, int blocks, cudaStream_t stream) {
+  if (sizeof(T) == 2 && (p.d & (p.d - 1)) != 0) return cudaErrorInvalidValue;
+  switch (p.d) {
+    case 64: prologue_kernel<T, 64><<<blocks, 256, 0, stream>>>(p); break;
+    case 128: prologue_kernel<T, 128><<<blocks, 256, 0, stream>>>(p); break;
+    case 256: prologue_kernel<T, 256><<<blocks, 256, 0, stream>>>(p); break;
+    case 512: prologue_kernel<T, 512><<<blocks, 256, 0, stream>>>(p); break;
+    case 192: prologue_kernel<T, 192><<<blocks, 256, 0, stream>>>(p); break;
+    case 320: prologue_kernel<T, 320><<<blocks, 256, 0, stream>>>(p); break;
+    case 384: prologue_kernel<T, 384><<<blocks, 256, 0, stream>>>(p); break;
+    case 448: prologue_kernel<T, 448><<<blocks, 256, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_key_prep_t(const KeyPrepArgs& k, int blocks, cudaStream_t stream) {
+  if (sizeof(T) == 2 && (k.d & (k.d - 1)) != 0) return cudaErrorInvalidValue;
+  switch (k.d) {
+    case 64: key_prep_kernel<T, 64><<<blocks, 256, 0, stream>>>(k); break;
+    case 128: key_prep_kernel<T, 128><<<blocks, 256, 0, stream>>>(k); break;
+    case 256: key_prep_kernel<T, 256><<<blocks, 256, 0, stream>>>(k); break;
+    case 512: key_prep_kernel<T, 512><<<blocks, 256, 0, stream>>>(k); break;
+    case 192: key_prep_kernel<T, 192><<<blocks, 256, 0, stream>>>(k); break;
+    case 320: key_prep_kernel<T, 320><<<blocks, 256, 0, stream>>>(k); break;
+    case 384: key_prep_kernel<T, 384><<<blocks, 256, 0, stream>>>(k); break;
+    case 448: key_prep_kernel<T, 448><<<blocks, 256, 0, stream>>>(k); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -260,24 +346,16 @@ cudaError_t launch_prologue(const PrologueArgs& p, bool bf16, cudaStream_t strea
   const int heads = p.Hq + p.Hkv + (p.global ? 0 : p.Hkv);
   const long long warps = (long long)p.B * p.C * heads;
   const int blocks = int((warps * 32 + 255) / 256);
-  if (bf16)
-    prologue_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(p);
-  else
-    prologue_kernel<float><<<blocks, 256, 0, stream>>>(p);
   count_launches(1);
-  return cudaGetLastError();
+  return bf16 ? launch_prologue_t<__nv_bfloat16>(p, blocks, stream) : launch_prologue_t<float>(p, blocks, stream);
 }
 
 cudaError_t launch_key_prep(const KeyPrepArgs& k, bool bf16, cudaStream_t stream) {
   const int rows = (k.global ? k.max_prefix : 0) + k.Tpad;
   const long long warps = (long long)k.B * k.Hkv * rows;
   const int blocks = int((warps * 32 + 255) / 256);
-  if (bf16)
-    key_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(k);
-  else
-    key_prep_kernel<float><<<blocks, 256, 0, stream>>>(k);
   count_launches(1);
-  return cudaGetLastError();
+  return bf16 ? launch_key_prep_t<__nv_bfloat16>(k, blocks, stream) : launch_key_prep_t<float>(k, blocks, stream);
 }
 
 }  // namespace canvas

@@ -6,8 +6,10 @@
 // argmax; the CTAs swap their partial states through distributed shared
 // memory and every CTA merges them in rank order (so all agree bit for bit).
 // CTA 0 then writes the row's entropy / confidence / argmax and the
-// commit-or-renoise decision; every CTA re-reads its slice (L2-resident) and
-// writes the probabilities.
+// commit-or-renoise decision; every CTA writes the probabilities of its
+// slice.  bf16 logits: each thread holds its part of the slice in registers
+// (up to 16 x 16 bytes, all loads in flight at once), so the logits are read
+// from HBM exactly once.  fp32 logits (small vocabularies) re-read the slice.
 //
 // Method: AI Trends summary of a DiffusionGemma 26B notebook
 // (aitrends.kr/articles/94089), "섹션별 상세", sampling-loop paragraph (entropy
@@ -54,28 +56,33 @@ __device__ __forceinline__ void state_merge(RowState& a, const RowState& b) {
   }
   const float M = fmaxf(a.m, b.m);
   const float da = a.m - M, db = b.m - M;
-  const float sa = exp2f(da), sb = exp2f(db);
+  const float sa = ex2_approx(da), sb = ex2_approx(db);
   a.T = sa * (a.T + da * a.Z) + sb * (b.T + db * b.Z);
   a.Z = sa * a.Z + sb * b.Z;
   a.m = M;
 }
 
-// Fold a group of 8 values (already scaled to base 2 in y[]) into s.
-__device__ __forceinline__ void state_add8(RowState& s, const float (&x)[8], const float (&y)[8], int idx0) {
-  float vmax = y[0];
+// Fold a group of 8 raw logits x[] (indices idx0 .. idx0+7, increasing within
+// a thread) into s; y = x * ysc is the base-2 scaled logit.  The argmax and
+// the running maximum are updated from the group maximum, so the per-element
+// work is one max, one fused multiply-add, one exponential and two sums.
+__device__ __forceinline__ void state_add8(RowState& s, const float (&x)[8], float ysc, int idx0) {
+  float xm = x[0];
 #pragma unroll
-  for (int j = 1; j < 8; ++j) vmax = fmaxf(vmax, y[j]);
+  for (int j = 1; j < 8; ++j) xm = fmaxf(xm, x[j]);
+  if (xm > s.bx) {  // strict: an earlier (lower) index keeps a tie
+    int jm = 7;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (x[j] > s.bx) {  // strict: indices increase within a thread
-      s.bx = x[j];
-      s.bi = idx0 + j;
-    }
+    for (int j = 6; j >= 0; --j)
+      if (x[j] == xm) jm = j;
+    s.bx = xm;
+    s.bi = idx0 + jm;
   }
+  const float vmax = xm * ysc;
   if (vmax > s.m) {
     if (s.Z != 0.f) {
       const float dm = s.m - vmax;
-      const float sc = exp2f(dm);
+      const float sc = ex2_approx(dm);
       s.T = sc * (s.T + dm * s.Z);
       s.Z *= sc;
     }
@@ -83,8 +90,8 @@ __device__ __forceinline__ void state_add8(RowState& s, const float (&x)[8], con
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float t = y[j] - s.m;
-    const float e = exp2f(t);
+    const float t = fmaf(x[j], ysc, -s.m);
+    const float e = ex2_approx(t);
     s.Z += e;
     s.T = fmaf(t, e, s.T);
   }
@@ -127,12 +134,163 @@ __device__ __forceinline__ uint64_t renoise_key(uint64_t seed, uint32_t step, ui
   return splitmix_out(splitmix_out(splitmix_out(seed) ^ uint64_t(step)) ^ uint64_t(row));
 }
 
+// Row outputs and the commit / renoise decision (per-position commit mode).
+__device__ __forceinline__ void row_decision(const SampleArgs& a, int row, const RowState& t) {
+  const float H = logf(t.Z) - kLn2 * t.T / t.Z;
+  const float conf = 1.0f / t.Z;
+  a.entropy[row] = H;
+  a.confidence[row] = conf;
+  a.argmax[row] = t.bi;
+  if (a.commit_mode == 0) {
+    const bool fr = a.frozen != nullptr && a.frozen[row] != 0;
+    const bool commit = fr || (H < a.bound);
+    int tok;
+    if (fr)
+      tok = a.frozen_tokens[row];
+    else if (commit)
+      tok = t.bi;
+    else
+      tok = int(renoise_key(a.seed, a.step, uint32_t(row)) % uint64_t(a.V));
+    a.tokens[row] = tok;
+    a.commit_mask[row] = commit ? 1 : 0;
+  }
+}
+
+// Warp, CTA and cluster reduction of the row state (fixed order: every CTA of
+// the cluster ends with the same bits).  Returns the row's final state.
+template <int kThreads>
+__device__ __forceinline__ RowState reduce_row(RowState s, RowState* warp_part, float (*cl_part)[5],
+                                               uint32_t rank, uint32_t csize) {
+  constexpr int kWarps = kThreads / 32;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    RowState o;
+    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+    o.Z = __shfl_xor_sync(0xffffffffu, s.Z, off);
+    o.T = __shfl_xor_sync(0xffffffffu, s.T, off);
+    o.bx = __shfl_xor_sync(0xffffffffu, s.bx, off);
+    o.bi = __shfl_xor_sync(0xffffffffu, s.bi, off);
+    RowState lo = (threadIdx.x & off) ? o : s;
+    const RowState hi = (threadIdx.x & off) ? s : o;
+    state_merge(lo, hi);
+    s = lo;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) warp_part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RowState t = warp_part[0];
+    for (int w = 1; w < kWarps; ++w) state_merge(t, warp_part[w]);
+    const uint32_t local = smem_u32(&cl_part[rank][0]);
+    for (uint32_t dst = 0; dst < csize; ++dst) {
+      const uint32_t ra = mapa_shared(local, dst);
+      st_cluster_f32(ra + 0, t.m);
+      st_cluster_f32(ra + 4, t.Z);
+      st_cluster_f32(ra + 8, t.T);
+      st_cluster_f32(ra + 12, t.bx);
+      st_cluster_u32(ra + 16, uint32_t(t.bi));
+    }
+  }
+  cluster_sync_all();
+  RowState t;
+  state_init(t);
+  for (uint32_t r = 0; r < csize; ++r) {
+    RowState o;
+    o.m = cl_part[r][0];
+    o.Z = cl_part[r][1];
+    o.T = cl_part[r][2];
+    o.bx = cl_part[r][3];
+    o.bi = int(__float_as_uint(cl_part[r][4]));
+    state_merge(t, o);
+  }
+  return t;
+}
+
+// bf16 logits, the slice staged in shared memory by one bulk copy (up to
+// 64 KB): the HBM read is issued at once and overlaps the cluster start-up,
+// both passes read shared memory, and three CTAs fit on an SM so one CTA's
+// loads overlap another's arithmetic.
+constexpr int kSmemSliceBytes = 65536;
+
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a,
+                                                                     const __nv_bfloat16* __restrict__ logits) {
+  constexpr int kWarps = kThreads / 32;
+  extern __shared__ __align__(128) uint8_t slice_raw[];
+  __shared__ RowState warp_part[kWarps];
+  __shared__ float cl_part[kMaxSampleCluster][5];
+  __shared__ uint64_t full;
+  __shared__ int abort_flag;
+  const int row = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t csize = gridDim.x;
+  const long long c0 = (long long)rank * a.chunk;
+  const long long c1 = min((long long)a.V, c0 + a.chunk);
+  const int n = c1 > c0 ? int(c1 - c0) : 0;  // a multiple of 8
+  const __nv_bfloat16* src = logits + (long long)row * a.V + c0;
+  const __nv_bfloat16* slice = reinterpret_cast<const __nv_bfloat16*>(slice_raw);
+  if (threadIdx.x == 0) {
+    mbar_init(&full, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+    mbar_arrive_expect_tx(&full, uint32_t(n) * 2u);
+    for (int off = 0; off < n; off += 8192)  // 16 KB pieces
+      bulk_load(slice_raw + off * 2, src + off, uint32_t(min(8192, n - off)) * 2u, &full);
+  }
+  // every CTA of the cluster is running before any DSMEM store (in reduce_row)
+  cluster_sync_all();
+  // on a timeout the status word is set and the CTA carries on, so that no
+  // peer waits for it at a cluster barrier
+  mbar_wait(&full, 0, &abort_flag);
+  const float ysc = a.inv_temp * kLog2e;
+  RowState s;
+  state_init(s);
+  for (int i = threadIdx.x * 8; i < n; i += kThreads * 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+    state_add8(s, x, ysc, int(c0) + i);
+  }
+  const RowState t = reduce_row<kThreads>(s, warp_part, cl_part, rank, csize);
+  if (threadIdx.x == 0 && rank == 0) row_decision(a, row, t);
+  const float M = t.m;
+  const float invZ = 1.0f / t.Z;
+  for (int i = threadIdx.x * 8; i < n; i += kThreads * 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      p[2 * j] = ex2_approx(fmaf(__uint_as_float(w[j] << 16), ysc, -M)) * invZ;
+      p[2 * j + 1] = ex2_approx(fmaf(__uint_as_float(w[j] & 0xffff0000u), ysc, -M)) * invZ;
+    }
+    const long long o = (long long)row * a.V + c0 + i;
+    if (a.probs_bf16) {
+      uint4 q;
+      q.x = pack_bf16x2(p[0], p[1]);
+      q.y = pack_bf16x2(p[2], p[3]);
+      q.z = pack_bf16x2(p[4], p[5]);
+      q.w = pack_bf16x2(p[6], p[7]);
+      *reinterpret_cast<uint4*>(a.probs_bf16 + o) = q;
+    }
+    if (a.probs_f32) {
+      float4* q = reinterpret_cast<float4*>(a.probs_f32 + o);
+      q[0] = make_float4(p[0], p[1], p[2], p[3]);
+      q[1] = make_float4(p[4], p[5], p[6], p[7]);
+    }
+  }
+}
+
 template <typename T, int kThreads>
 __global__ void __launch_bounds__(kThreads) sample_rows_kernel(SampleArgs a, const T* __restrict__ logits) {
   constexpr int kWarps = kThreads / 32;
   __shared__ RowState warp_part[kWarps];
   __shared__ float cl_part[kMaxSampleCluster][5];
-  __shared__ RowState final_state;
 
   const int row = blockIdx.y;
   const uint32_t rank = cluster_ctarank();
@@ -148,88 +306,20 @@ __global__ void __launch_bounds__(kThreads) sample_rows_kernel(SampleArgs a, con
   state_init(s);
   // pass 1: statistics
   for (long long i = c0 + (long long)threadIdx.x * 8; i < c1; i += (long long)kThreads * 8) {
-    float x[8], y[8];
+    float x[8];
     Vec8<T>::load(lrow + i, x);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = x[j] * ysc;
-    state_add8(s, x, y, int(i));
+    state_add8(s, x, ysc, int(i));
   }
-  // warp reduce (fixed butterfly order)
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    RowState o;
-    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
-    o.Z = __shfl_xor_sync(0xffffffffu, s.Z, off);
-    o.T = __shfl_xor_sync(0xffffffffu, s.T, off);
-    o.bx = __shfl_xor_sync(0xffffffffu, s.bx, off);
-    o.bi = __shfl_xor_sync(0xffffffffu, s.bi, off);
-    // lanes merge in a symmetric way so that both partners hold the same value
-    RowState lo = (threadIdx.x & off) ? o : s;
-    const RowState hi = (threadIdx.x & off) ? s : o;
-    state_merge(lo, hi);
-    s = lo;
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) warp_part[warp] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    RowState t = warp_part[0];
-    for (int w = 1; w < kWarps; ++w) state_merge(t, warp_part[w]);
-    // send this CTA's partial to every CTA of the cluster, slot = rank
-    const uint32_t local = smem_u32(&cl_part[rank][0]);
-    for (uint32_t dst = 0; dst < csize; ++dst) {
-      const uint32_t ra = mapa_shared(local, dst);
-      st_cluster_f32(ra + 0, t.m);
-      st_cluster_f32(ra + 4, t.Z);
-      st_cluster_f32(ra + 8, t.T);
-      st_cluster_f32(ra + 12, t.bx);
-      st_cluster_u32(ra + 16, uint32_t(t.bi));
-    }
-  }
-  cluster_sync_all();
-  if (threadIdx.x == 0) {
-    RowState t;
-    state_init(t);
-    for (uint32_t r = 0; r < csize; ++r) {
-      RowState o;
-      o.m = cl_part[r][0];
-      o.Z = cl_part[r][1];
-      o.T = cl_part[r][2];
-      o.bx = cl_part[r][3];
-      o.bi = int(__float_as_uint(cl_part[r][4]));
-      state_merge(t, o);
-    }
-    final_state = t;
-    if (rank == 0) {
-      const float H = logf(t.Z) - kLn2 * t.T / t.Z;
-      const float conf = 1.0f / t.Z;
-      a.entropy[row] = H;
-      a.confidence[row] = conf;
-      a.argmax[row] = t.bi;
-      if (a.commit_mode == 0) {
-        const bool fr = a.frozen != nullptr && a.frozen[row] != 0;
-        const bool commit = fr || (H < a.bound);
-        int tok;
-        if (fr)
-          tok = a.frozen_tokens[row];
-        else if (commit)
-          tok = t.bi;
-        else
-          tok = int(renoise_key(a.seed, a.step, uint32_t(row)) % uint64_t(a.V));
-        a.tokens[row] = tok;
-        a.commit_mask[row] = commit ? 1 : 0;
-      }
-    }
-  }
-  __syncthreads();
-  const float M = final_state.m;
-  const float invZ = 1.0f / final_state.Z;
+  const RowState t = reduce_row<kThreads>(s, warp_part, cl_part, rank, csize);
+  if (threadIdx.x == 0 && rank == 0) row_decision(a, row, t);
+  const float M = t.m;
+  const float invZ = 1.0f / t.Z;
   // pass 2: probabilities
   for (long long i = c0 + (long long)threadIdx.x * 8; i < c1; i += (long long)kThreads * 8) {
     float x[8], p[8];
     Vec8<T>::load(lrow + i, x);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) p[j] = exp2f(x[j] * ysc - M) * invZ;
+    for (int j = 0; j < 8; ++j) p[j] = ex2_approx(fmaf(x[j], ysc, -M)) * invZ;
     const long long o = (long long)row * a.V + i;
     if (a.probs_bf16) {
       uint4 u;
@@ -284,11 +374,22 @@ cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, c
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (bf16)
-    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<__nv_bfloat16, kThreads>, a,
-                           static_cast<const __nv_bfloat16*>(logits));
-  else
+  const __nv_bfloat16* lb = static_cast<const __nv_bfloat16*>(logits);
+  if (bf16 && size_t(a.chunk) * 2 <= size_t(kSmemSliceBytes)) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemSliceBytes);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    cfg.dynamicSmemBytes = size_t(a.chunk) * 2;
+    e = cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads>, a, lb);
+  } else if (bf16) {
+    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<__nv_bfloat16, kThreads>, a, lb);
+  } else {
     e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<float, kThreads>, a, static_cast<const float*>(logits));
+  }
   if (e != cudaSuccess) return e;
   count_launches(1);
   if (a.commit_mode == 1) {
