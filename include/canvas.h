@@ -78,7 +78,7 @@ typedef enum {
  *         of sequence b (tokens p*page_tokens ...).  Entries for pages that hold
  *         no visible token may be -1; entries that are read must lie in
  *         [0, num_pages), else the call records CANVAS_ERR_BOUNDS.
- * page_tokens must be a multiple of 64 for bf16 calls (of 16 for fp32 calls).
+ * page_tokens must be a multiple of 64 for bf16 calls (any size for fp32 calls).
  */
 typedef struct {
   const void* k_pool;
@@ -113,10 +113,7 @@ size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, i
  *   W_q      [Hq*d, D]            dtype;  q = x W_q^T
  *   W_k      [Hkv*d, D]           dtype;  k = x W_k^T
  *   W_v      [Hkv*d, D] or NULL   dtype;  NULL only on global layers (W_v = W_k)
- *   gamma_q, gamma_k [d] fp32     QK-norm weights.  On global layers gamma_k
- *                                 must be constant-valued (the pages report
- *                                 constant learned vectors); a kernel checks
- *                                 it and records CANVAS_ERR_UNSUPPORTED.
+ *   gamma_q, gamma_k [d] fp32     QK-norm weights
  *   eps                           rms epsilon, added to ||x||_2
  *   freq     [d/2] fp32           RoPE spectrum; zero entries are not rotated
  *   layer_type                    canvas_layer_type
@@ -129,10 +126,11 @@ size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, i
  *   window                        sliding layers: a canvas row at position p
  *                                 sees prefix keys j >= p - window; <= 0 means
  *                                 the whole prefix.  Ignored on global layers.
- *   scale                         multiplies q.k (1.0: the QK norm already
+ *   scale                         multiplies q.k, > 0 (1.0: the QK norm already
  *                                 fixes the temperature)
  *   v_unit_rms                    0 (default).  1 on a global layer: value =
- *                                 sqrt(d) * r / (||r|| + eps)
+ *                                 sqrt(d) * r / (||r|| + eps) (the scalar is
+ *                                 applied in fp32 to each key's softmax weight)
  *   out      [B, C, Hq*d] dtype   heads concatenated, 'n l h -> l (n h)'
  *   lse      [B, C, Hq] fp32 or NULL   natural-log softmax normaliser
  *   workspace, ws_bytes           >= canvas_attention_workspace_size(...),
@@ -164,7 +162,7 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  * (low-confidence tokens swapped for random tokens), and the self-conditioning
  * glossary entry of [AIT] (expected embedding P.E of the softmax).
  *
- *   logits   [rows, V] dtype      rows = B*C positions
+ *   logits   [rows, V] dtype      rows = B*C positions; 16-byte aligned
  *   E        [V, D] dtype         embedding table (row-major)
  *   entropy_bound                 commit iff entropy < bound (nats, strict)
  *   seed, step                    renoise key = m(m(m(seed) ^ step) ^ row),
@@ -180,7 +178,7 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  *   commit_mask [rows] uint8      out: 1 = committed
  *   entropy, confidence [rows] fp32  out: -sum p ln p, max p
  *   argmax   [rows] int32 or NULL out: lowest index of the largest logit
- *   probs_out [rows, V] or NULL   out: softmax, in probs_dtype
+ *   probs_out [rows, V] or NULL   out: softmax, in probs_dtype; 16-byte aligned
  *   probs_dtype                   CANVAS_BF16 or CANVAS_FP32
  *   soft_emb [rows, D] fp32       out: P.E.  bf16 calls multiply the bf16
  *                                 probabilities; fp32 calls the fp32 ones.
