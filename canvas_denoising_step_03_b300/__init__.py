@@ -38,6 +38,7 @@ EXPORTED = [
     "canvas_attention_workspace_size", "canvas_attention", "canvas_sample_workspace_size", "canvas_sample",
     "canvas_gemm_workspace_size", "canvas_gemm_bf16", "canvas_last_error", "canvas_device_status",
     "canvas_version", "canvas_profile_events", "canvas_kernel_launches", "canvas_gemm_bf16_noalloc",
+    "canvas_embed_input", "canvas_cast_bf16",
 ]
 
 # size of the static scratch behind canvas_gemm_bf16_noalloc (include/canvas.h)
@@ -82,6 +83,10 @@ def _load(path: str = LIB_PATH):
     lib.canvas_gemm_bf16.restype = I
     lib.canvas_gemm_bf16_noalloc.argtypes = [P, P, I, P, I, I, I, I, P]
     lib.canvas_gemm_bf16_noalloc.restype = I
+    lib.canvas_embed_input.argtypes = [P, P, P, I, I, I, P, P, P]
+    lib.canvas_embed_input.restype = I
+    lib.canvas_cast_bf16.argtypes = [P, P, Z, P]
+    lib.canvas_cast_bf16.restype = I
     lib.canvas_last_error.argtypes = []
     lib.canvas_last_error.restype = ctypes.c_char_p
     lib.canvas_device_status.argtypes = [P]
@@ -203,6 +208,19 @@ def canvas_gemm_bf16_noalloc(A, B, b_layout, C, accumulate, stream=None):
     N = B.shape[0] if b_layout == 0 else B.shape[1]
     _check(lib.canvas_gemm_bf16_noalloc(_ptr(A), _ptr(B), int(b_layout), _ptr(C), M, N, K, int(accumulate),
                                         _stream(stream)))
+
+
+def canvas_embed_input(tokens, E, soft_emb, x, x32=None, stream=None):
+    """x = bf16(E[tokens] + soft_emb), x32 = the fp32 sum (soft_emb, x32 may be None)."""
+    rows = tokens.numel()
+    V, D = E.shape
+    _check(lib.canvas_embed_input(_ptr(tokens), _ptr(E), _ptr(soft_emb), rows, D, V, _ptr(x), _ptr(x32),
+                                  _stream(stream)))
+
+
+def canvas_cast_bf16(src, dst, stream=None):
+    """dst (bf16) = src (fp32), element for element."""
+    _check(lib.canvas_cast_bf16(_ptr(src), _ptr(dst), src.numel(), _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

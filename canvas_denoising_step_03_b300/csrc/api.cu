@@ -308,6 +308,30 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
   return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ loop glue
+canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const float* soft_emb, int rows, int D,
+                                 int V, void* x, float* x32, canvas_stream_t stream) {
+  if (!tokens || !E || !x) return fail(CANVAS_ERR_ARG, "canvas_embed_input: null pointer");
+  if (rows < 1 || D < 1 || V < 1) return fail(CANVAS_ERR_ARG, "canvas_embed_input: bad shape");
+  if (D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_embed_input: D must be a multiple of 8");
+  if ((reinterpret_cast<uintptr_t>(E) | reinterpret_cast<uintptr_t>(soft_emb) | reinterpret_cast<uintptr_t>(x) |
+       reinterpret_cast<uintptr_t>(x32)) %
+          16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_embed_input: E, soft_emb, x and x32 must be 16-byte aligned");
+  CANVAS_CUDA(launch_embed_input(tokens, E, soft_emb, rows, D, V, x, x32, reinterpret_cast<cudaStream_t>(stream)));
+  return CANVAS_OK;
+}
+
+canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stream_t stream) {
+  if (!in || !out) return fail(CANVAS_ERR_ARG, "canvas_cast_bf16: null pointer");
+  if (n % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_cast_bf16: n must be a multiple of 8");
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_cast_bf16: pointers must be 16-byte aligned");
+  if (n == 0) return CANVAS_OK;
+  CANVAS_CUDA(launch_cast_bf16(in, out, (long long)n, reinterpret_cast<cudaStream_t>(stream)));
+  return CANVAS_OK;
+}
+
 // ------------------------------------------------------------------ GEMM without a workspace
 // The split-K scratch of canvas_gemm_bf16_noalloc: one static device array,
 // shared by every call on a device.  Host code cannot use the symbol as a

@@ -157,4 +157,9 @@ size_t attention_tc_smem_bytes(int d);
 cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream);
 cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream);
 
+// ----------------------------------------------------------------- loop glue
+cudaError_t launch_embed_input(const int32_t* tokens, const void* E, const float* soft, int rows, int D, int V,
+                               void* x, float* x32, cudaStream_t stream);
+cudaError_t launch_cast_bf16(const float* in, void* out, long long n, cudaStream_t stream);
+
 }  // namespace canvas

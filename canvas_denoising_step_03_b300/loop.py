@@ -1,0 +1,135 @@
+"""A batched multi-layer denoising loop built only from the library's C-ABI
+calls (argument marshalling and buffer management here; every arithmetic step
+runs in the library's kernels).
+
+One step, for B canvases of C tokens:
+
+1. ``canvas_embed_input``: v = E[tokens] + soft_emb of the previous step
+   (bf16 copy for the layers, fp32 copy as the residual stream);
+2. per layer: ``canvas_attention`` on the bf16 stream, then
+   ``canvas_gemm_bf16`` adds out W_o^T to the fp32 stream and
+   ``canvas_cast_bf16`` refreshes the bf16 copy;
+3. tied LM head: ``canvas_gemm_bf16`` computes x E^T (fp32), cast to bf16;
+4. ``canvas_sample`` with the step index; positions committed in earlier
+   steps stay frozen with their tokens.
+
+The method's sampling loop and self-conditioning are described in the AI
+Trends summary of a DiffusionGemma 26B notebook (aitrends.kr/articles/94089),
+section "섹션별 상세" (sampling-loop paragraph) and glossary "자기 조건화".
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (CANVAS_BF16, CANVAS_LAYER_GLOBAL, CANVAS_LAYER_SLIDING, canvas_attention,
+               canvas_attention_workspace_size, canvas_cast_bf16, canvas_embed_input, canvas_gemm_bf16,
+               canvas_gemm_workspace_size, canvas_sample, canvas_sample_workspace_size, make_kv_cache, workspace)
+
+
+def _bf16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class CanvasLoop:
+    """Device state of the loop for one set of inputs (the layout of
+    ``canvas_workloads.LoopInputs``: bf16 bit patterns, caches holding
+    positions cache_lo .. prefix-1 of every sequence)."""
+
+    def __init__(self, inp, device="cuda", page_tokens: int = 64, seed_pages: int = 1234):
+        import canvas_workloads as wl  # shapes and page tables of the seeded inputs
+        cfg = inp.cfg
+        self.cfg, self.dev = cfg, device
+        B, C, D, V = cfg.B, cfg.C, cfg.D, cfg.V
+        R = B * C
+        self.layers = []
+        attn_ws = 0
+        for k, L in enumerate(inp.layers):
+            lc = L.cfg
+            table, npages = wl.page_layout_range(B, L.cache_lo, cfg.prefix, page_tokens, seed=seed_pages + k)
+            kp = _bf16(wl.scatter_pages_range(L.cache_k, L.cache_lo, table, npages, page_tokens), device)
+            vp = None if L.cache_v is None else _bf16(
+                wl.scatter_pages_range(L.cache_v, L.cache_lo, table, npages, page_tokens), device)
+            bt = torch.from_numpy(table).to(device)
+            layer = dict(cfg=lc, W_q=_bf16(L.W_q, device), W_k=_bf16(L.W_k, device),
+                         W_v=None if L.W_v is None else _bf16(L.W_v, device), W_o=_bf16(L.W_o, device),
+                         gamma_q=torch.from_numpy(L.gamma_q).to(device), gamma_k=torch.from_numpy(L.gamma_k).to(device),
+                         freq=torch.from_numpy(L.freq).to(device), k_pool=kp, v_pool=vp, table=bt,
+                         kv=make_kv_cache(kp, vp, bt, page_tokens),
+                         type=CANVAS_LAYER_GLOBAL if lc.layer == "global" else CANVAS_LAYER_SLIDING,
+                         out=torch.empty((B, C, lc.Hq * lc.d), dtype=torch.bfloat16, device=device))
+            self.layers.append(layer)
+            attn_ws = max(attn_ws, canvas_attention_workspace_size(CANVAS_BF16, B, C, D, lc.Hq, lc.Hkv, lc.d,
+                                                                   cfg.prefix, layer["type"]))
+        self.prefix_len = torch.full((B,), cfg.prefix, dtype=torch.int32, device=device)
+        self.E = _bf16(inp.E, device)
+        self.tokens = torch.from_numpy(inp.tokens0.astype(np.int32)).to(device)
+        self.x = torch.empty((B, C, D), dtype=torch.bfloat16, device=device)
+        self.x32 = torch.empty((R, D), dtype=torch.float32, device=device)
+        self.logits32 = torch.empty((R, V), dtype=torch.float32, device=device)
+        self.logits = torch.empty((R, V), dtype=torch.bfloat16, device=device)
+        self.soft = torch.zeros((R, D), dtype=torch.float32, device=device)
+        self.frozen = torch.zeros(R, dtype=torch.uint8, device=device)
+        self.mask = torch.zeros(R, dtype=torch.uint8, device=device)
+        self.next_tokens = torch.empty(R, dtype=torch.int32, device=device)
+        self.entropy = torch.empty(R, dtype=torch.float32, device=device)
+        self.conf = torch.empty(R, dtype=torch.float32, device=device)
+        self.argmax = torch.empty(R, dtype=torch.int32, device=device)
+        self.attn_ws = workspace(attn_ws, device)
+        gws = max([canvas_gemm_workspace_size(R, D, L["cfg"].Hq * L["cfg"].d) for L in self.layers] +
+                  [canvas_gemm_workspace_size(R, V, D)])
+        self.gemm_ws = workspace(gws, device)
+        self.samp_ws = workspace(canvas_sample_workspace_size(CANVAS_BF16, R, V, D), device)
+        self.step_index = 0
+
+    # ---- the stages of a step (each one C-ABI call or two)
+    def embed(self, tokens: torch.Tensor, soft):
+        """x, x32 = E[tokens] + soft (soft None: no self-conditioning input)."""
+        canvas_embed_input(tokens, self.E, soft, self.x, self.x32)
+
+    def attention(self, k: int, x: torch.Tensor) -> torch.Tensor:
+        """Layer k's attention on the bf16 canvas stream x [B, C, D]."""
+        cfg, L = self.cfg, self.layers[k]
+        lc = L["cfg"]
+        canvas_attention(x, L["W_q"], L["W_k"], L["W_v"], lc.Hq, lc.Hkv, lc.d, L["gamma_q"], L["gamma_k"], lc.eps,
+                         L["freq"], L["type"], L["kv"], self.prefix_len, cfg.prefix, lc.window, 1.0, 0, L["out"],
+                         None, self.attn_ws)
+        return L["out"]
+
+    def residual(self, k: int, out: torch.Tensor, x32: torch.Tensor, x: torch.Tensor):
+        """x32 += out W_o^T (fp32), x = bf16(x32)."""
+        R = self.cfg.B * self.cfg.C
+        canvas_gemm_bf16(out.view(R, -1), self.layers[k]["W_o"], 0, x32, 1, self.gemm_ws)
+        canvas_cast_bf16(x32, x)
+
+    def head(self, x: torch.Tensor) -> torch.Tensor:
+        """bf16 logits of the tied LM head, x E^T."""
+        R = self.cfg.B * self.cfg.C
+        canvas_gemm_bf16(x.view(R, -1), self.E, 0, self.logits32, 0, self.gemm_ws)
+        canvas_cast_bf16(self.logits32, self.logits)
+        return self.logits
+
+    def sample(self, logits: torch.Tensor, step: int, frozen: torch.Tensor, frozen_tokens: torch.Tensor):
+        """The sampler of step ``step``; outputs in next_tokens, mask, entropy,
+        conf, argmax, soft."""
+        cfg = self.cfg
+        canvas_sample(logits, self.E, cfg.bound, cfg.seed, step, 1.0, 0, cfg.C, frozen, frozen_tokens,
+                      self.next_tokens, self.mask, self.entropy, self.conf, self.argmax, None, CANVAS_BF16,
+                      self.soft, self.samp_ws)
+
+    def step(self, keep_attn: bool = False):
+        """Run one denoising step on the loop's own state; returns the
+        attention outputs if asked."""
+        self.embed(self.tokens, self.soft if self.step_index > 0 else None)
+        outs = []
+        for k in range(len(self.layers)):
+            out = self.attention(k, self.x)
+            if keep_attn:
+                outs.append(out.clone())
+            self.residual(k, out, self.x32, self.x)
+        self.sample(self.head(self.x), self.step_index, self.frozen, self.tokens)
+        # committed positions stay frozen with their tokens in the next step
+        self.tokens, self.next_tokens = self.next_tokens, self.tokens
+        self.frozen.copy_(self.mask)
+        self.step_index += 1
+        return outs

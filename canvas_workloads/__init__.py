@@ -20,7 +20,8 @@ Shapes and distributions follow the five workloads of the canvas step:
 * ``sampler`` -- 256 positions x vocab 262144 bf16 logits, half peaked rows,
   half flat rows, E[262144 x 2816] ~ N(0, 0.02^2) (seed 7).
 * ``loop``    -- 4 canvases x 256, 5 sliding + 1 global layers, prefix swept
-  over 1K/8K/32K/128K, 48 steps (seed 11).
+  over 1K/8K/32K/128K, 48 steps (seed 11); a small loop of the same
+  structure for step-by-step parity.
 """
 from __future__ import annotations
 
@@ -284,22 +285,144 @@ def make_sample_inputs(cfg: SampleConfig, with_E: bool = True) -> SampleInputs:
 
 @dataclass(frozen=True)
 class LoopConfig:
+    """A batch of canvases denoised for ``steps`` steps through a stack of
+    ``n_sliding`` sliding-window layers (shapes of ``sliding``) followed by
+    ``n_global`` global layers (shapes of ``global_``), a tied LM head and the
+    sampler.  Each layer draws its own weights, QK-norm constants and cache."""
     name: str
     B: int
     C: int
     prefix: int
     steps: int
-    n_sliding: int
-    n_global: int
     V: int
     D: int
     seed: int
+    sliding: AttnConfig
+    global_: AttnConfig
+    n_sliding: int = 5
+    n_global: int = 1
     bound: float = 0.3
+    E_std: float = 0.02
+
+    def layer_cfgs(self):
+        out = []
+        for k in range(self.n_sliding + self.n_global):
+            t = self.sliding if k < self.n_sliding else self.global_
+            out.append(replace(t, name=f"{self.name}-L{k}", B=self.B, C=self.C, prefix=(self.prefix,) * self.B,
+                               D=self.D, seed=self.seed * 1000 + k))
+        return out
 
 
 def loop_config(prefix: int, B: int = 4, steps: int = 48) -> LoopConfig:
-    return LoopConfig(f"loop_p{prefix}", B=B, C=256, prefix=prefix, steps=steps, n_sliding=5,
-                      n_global=1, V=262144, D=2816, seed=11)
+    """The batched loop: 4 canvases of 256, 5 sliding layers (the sliding-layer
+    shapes) and 1 global layer (the global-layer shapes), vocab 262144."""
+    return LoopConfig(f"loop_p{prefix}", B=B, C=256, prefix=prefix, steps=steps, V=262144, D=2816, seed=11,
+                      sliding=SLIDING, global_=GLOBAL)
+
+
+def mini_loop_config(steps: int = 4) -> LoopConfig:
+    """A small loop of the same structure for step-by-step parity."""
+    sl = AttnConfig("mini-sliding", B=2, C=32, prefix=(160,), D=256, Hq=4, Hkv=2, d=64, layer="sliding",
+                    window=48, theta=1e4, rotary_fraction=1.0, dtype="bf16", seed=0)
+    gl = AttnConfig("mini-global", B=2, C=32, prefix=(160,), D=256, Hq=4, Hkv=1, d=128, layer="global",
+                    window=0, theta=1e6, rotary_fraction=0.25, dtype="bf16", seed=0)
+    return LoopConfig("mini_loop", B=2, C=32, prefix=160, steps=steps, V=4096, D=256, seed=21, sliding=sl,
+                      global_=gl, bound=0.3, E_std=0.3)
+
+
+@dataclass
+class LoopLayer:
+    cfg: AttnConfig
+    W_q: np.ndarray
+    W_k: np.ndarray
+    W_v: Optional[np.ndarray]
+    W_o: np.ndarray          # [D, Hq*d]
+    gamma_q: np.ndarray
+    gamma_k: np.ndarray
+    freq: np.ndarray
+    cache_lo: int            # first cached position (64-aligned); earlier pages are not allocated
+    cache_k: np.ndarray      # [B, Hkv, prefix - cache_lo, d]
+    cache_v: Optional[np.ndarray]
+
+
+@dataclass
+class LoopInputs:
+    cfg: LoopConfig
+    layers: list
+    E: np.ndarray            # [V, D]
+    tokens0: np.ndarray      # int32 [B*C]
+
+
+def make_loop_inputs(cfg: LoopConfig) -> LoopInputs:
+    """Seeded draws for the loop: per layer W ~ N(0, 1/D), W_o ~ N(0, 1/(Hq d)),
+    constant QK-norm vectors drawn U[0.5, 2], cache rows ~ N(0, 1) (sliding
+    layers keep only the pages a canvas row can see); E ~ N(0, E_std^2);
+    initial tokens uniform."""
+    layers = []
+    for lc in cfg.layer_cfgs():
+        rng = np.random.default_rng(lc.seed)
+        wstd = np.float32(1.0 / np.sqrt(lc.D))
+        W_q = rng.standard_normal((lc.Hq * lc.d, lc.D), dtype=np.float32) * wstd
+        W_k = rng.standard_normal((lc.Hkv * lc.d, lc.D), dtype=np.float32) * wstd
+        W_v = None
+        if lc.layer == "sliding":
+            W_v = rng.standard_normal((lc.Hkv * lc.d, lc.D), dtype=np.float32) * wstd
+        W_o = rng.standard_normal((lc.D, lc.Hq * lc.d), dtype=np.float32) * np.float32(1.0 / np.sqrt(lc.Hq * lc.d))
+        gq, gk = float(rng.uniform(0.5, 2.0)), float(rng.uniform(0.5, 2.0))
+        P = cfg.prefix
+        lo = 0
+        if lc.layer == "sliding" and lc.window > 0:
+            lo = max(0, P - lc.window) // 64 * 64
+        shape = (cfg.B, lc.Hkv, P - lo, lc.d)
+        ck = rng.standard_normal(shape, dtype=np.float32)
+        cv = rng.standard_normal(shape, dtype=np.float32) if lc.layer == "sliding" else None
+        layers.append(LoopLayer(cfg=lc, W_q=_store(W_q, "bf16"), W_k=_store(W_k, "bf16"),
+                                W_v=None if W_v is None else _store(W_v, "bf16"), W_o=_store(W_o, "bf16"),
+                                gamma_q=np.full(lc.d, gq, np.float32), gamma_k=np.full(lc.d, gk, np.float32),
+                                freq=rope_frequencies(lc.d, lc.theta, lc.rotary_fraction), cache_lo=lo,
+                                cache_k=_store(ck, "bf16"), cache_v=None if cv is None else _store(cv, "bf16")))
+    rng = np.random.default_rng(cfg.seed)
+    E = rng.standard_normal((cfg.V, cfg.D), dtype=np.float32) * np.float32(cfg.E_std)
+    tokens0 = rng.integers(0, cfg.V, size=cfg.B * cfg.C).astype(np.int32)
+    return LoopInputs(cfg=cfg, layers=layers, E=_store(E, "bf16"), tokens0=tokens0)
+
+
+def page_layout_range(B: int, lo: int, hi: int, page_tokens: int, seed: int = 1234, spare_pages: int = 2):
+    """Block table for caches that hold positions [lo, hi) of each sequence
+    (lo a multiple of page_tokens): logical pages below lo are -1, the others
+    a seeded permutation of physical pages.  Returns (table, num_pages)."""
+    first = lo // page_tokens
+    last = (hi + page_tokens - 1) // page_tokens
+    per = last - first
+    num_pages = B * per + spare_pages
+    perm = np.random.default_rng(seed).permutation(num_pages)
+    table = np.full((B, max(last, 1)), -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        for lp in range(first, last):
+            table[b, lp] = perm[k]
+            k += 1
+    return table, num_pages
+
+
+def scatter_pages_range(rows: np.ndarray, lo: int, table: np.ndarray, num_pages: int, page_tokens: int,
+                        fill: Optional[int] = None) -> np.ndarray:
+    """Rows [B, Hkv, n, d] holding positions lo .. lo+n-1 -> page pool."""
+    B, Hkv, n, d = rows.shape
+    if fill is None:
+        fill = 0x7FC0 if rows.dtype == np.uint16 else np.float32(np.nan)
+    pool = np.full((num_pages, Hkv, page_tokens, d), fill, dtype=rows.dtype)
+    for b in range(B):
+        for lp in range(table.shape[1]):
+            pid = table[b, lp]
+            if pid < 0:
+                continue
+            p0 = lp * page_tokens
+            a, z = max(p0, lo), min(p0 + page_tokens, lo + n)
+            if a >= z:
+                continue
+            pool[pid, :, a - p0:z - p0, :] = rows[b, :, a - lo:z - lo, :]
+    return pool
 
 
 __all__ = [
@@ -307,5 +430,6 @@ __all__ = [
     "TINY", "SLIDING", "GLOBAL", "TINY_SAMPLE", "FULL_SAMPLE",
     "make_attention_inputs", "make_sample_inputs", "make_logits", "page_layout",
     "scatter_pages", "rope_frequencies", "f32_to_bf16_bits", "bf16_bits_to_f32",
-    "as_f64", "loop_config", "replace",
+    "as_f64", "loop_config", "mini_loop_config", "make_loop_inputs", "LoopInputs", "LoopLayer",
+    "page_layout_range", "scatter_pages_range", "replace",
 ]

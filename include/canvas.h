@@ -216,6 +216,31 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
                                void* workspace, size_t ws_bytes, canvas_stream_t stream);
 
 /*
+ * canvas_embed_input -- the canvas input of a denoising step:
+ *   v[r, :] = E[tokens[r], :] + soft_emb[r, :]   (fp32)
+ *   x = bf16(v), x32 = v
+ * the embedding of the current tokens plus the self-conditioning soft
+ * embedding P.E of the previous step ([AIT] glossary, self-conditioning; the
+ * small MLP the page applies to P.E needs trained weights and is left to the
+ * caller).  Glue for callers that chain steps into a loop.
+ *   tokens   [rows] int32, each in [0, V) (else CANVAS_ERR_BOUNDS is recorded
+ *            and the row is zero)
+ *   E        [V, D] bf16, 16-byte aligned rows (D % 8 == 0)
+ *   soft_emb [rows, D] fp32 or NULL (step 0: no previous step)
+ *   x        [rows, D] bf16 out
+ *   x32      [rows, D] fp32 out or NULL (a residual stream kept in fp32)
+ */
+canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const float* soft_emb, int rows, int D,
+                                 int V, void* x, float* x32, canvas_stream_t stream);
+
+/*
+ * canvas_cast_bf16 -- out[i] = bf16(in[i]) (round to nearest even), n % 8 == 0,
+ * both 16-byte aligned.  Glue: an fp32 residual stream or fp32 logits become
+ * the bf16 operands of the next call.
+ */
+canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stream_t stream);
+
+/*
  * canvas_gemm_bf16_noalloc -- canvas_gemm_bf16 without a caller workspace.
  *
  * The pages have no counterpart to this call; it exists for callers that

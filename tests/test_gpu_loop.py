@@ -1,0 +1,220 @@
+"""The batched multi-layer denoising loop (canvas_denoising_step_03_b300.loop)
+against the fp64 oracle of the same loop (oracle/loop.py).
+
+A stack of random attention layers with these logit scales is chaotic: two
+runs whose first layer agrees to bf16 rounding part by orders of magnitude a
+few layers later (measured: 0.016, 0.03, 0.3, 2.1, 5.3, 6.8 max |err| over
+the six layers of the small loop).  So the loop is checked stage by stage:
+every stage of every step runs on the device from the oracle's own input to
+that stage (oracle values feed the device, never the reverse) and its output
+is held to the bar of that stage --
+  attention layer  |err| <= max(2e-2, one bf16 spacing of the value) +
+                   rounding slack, rel-Fro <= 5e-3 (the bars of
+                   test_gpu_attention.py; the activations of deeper layers
+                   reach |o| >= 8, where bf16 values are 1/16 apart);
+  residual add     the fp32 recursive-summation bound;
+  LM head          bf16 logits within one bf16 ulp plus that bound;
+  sampler          entropy within 1e-3 nats, tokens / commit masks bit-exact
+                   away from ties, soft embedding rel-Fro <= 5e-3.
+Free-running device trajectories are checked through what holds exactly:
+tokens are the argmax or the SplitMix64 renoise draw of their own decisions,
+committed positions stay committed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import canvas_workloads as wl
+from oracle import loop as oloop
+from oracle import splitmix
+
+pytestmark = pytest.mark.gpu
+TIE = 1e-6
+SLACK_EPS = 2.0 ** -17
+MAX_FRAC_OVER = 1e-3
+
+
+@pytest.fixture(scope="module")
+def cv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import canvas_denoising_step_03_b300 as cv
+    return cv
+
+
+def oracle_layers(inp):
+    f = lambda a: wl.as_f64(a, "bf16")  # noqa: E731
+    out = []
+    for L in inp.layers:
+        c = L.cfg
+        out.append(dict(W_q=f(L.W_q), W_k=f(L.W_k), W_v=None if L.W_v is None else f(L.W_v), W_o=f(L.W_o),
+                        gamma_q=L.gamma_q.astype(np.float64), gamma_k=L.gamma_k.astype(np.float64),
+                        freq=L.freq.astype(np.float64), eps=c.eps, Hq=c.Hq, Hkv=c.Hkv, d=c.d, layer=c.layer,
+                        window=c.window, prefix=inp.cfg.prefix,
+                        cache_k=oloop.dense_cache(f(L.cache_k), L.cache_lo, inp.cfg.prefix),
+                        cache_v=None if L.cache_v is None else oloop.dense_cache(f(L.cache_v), L.cache_lo,
+                                                                                inp.cfg.prefix)))
+    return out
+
+
+def to_bf16(a64, shape):
+    """Exact bf16 values (fp64) -> a device bf16 tensor."""
+    bits = wl.f32_to_bf16_bits(np.asarray(a64, np.float32))
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).reshape(shape)).cuda().view(torch.bfloat16)
+
+
+def bf16_ulp(a):
+    a = np.abs(np.asarray(a, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.ldexp(1.0, (e - 7).astype(int))
+
+
+U = 2.0 ** -24
+
+
+def gamma(K):
+    return K * U / (1 - K * U)
+
+
+def check_step(cv, run, ref, cfg, step, frozen, ftok, rows, run_wo, E_exact):
+    """Every stage of one step from the oracle's inputs; ``rows``: sampler rows
+    the oracle evaluated; run_wo / E_exact: exact W_o of each layer and E."""
+    B, C, D = cfg.B, cfg.C, cfg.D
+    R = B * C
+    report = []
+    for k in range(len(run.layers)):
+        # attention of layer k on the oracle's canvas stream
+        xk = to_bf16(oloop.bf16_round(ref["xs"][k]), (B, C, D))
+        got = run.attention(k, xk).float().cpu().numpy().astype(np.float64)
+        assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+        want, slack = ref["attn"][k], ref["slack"][k]
+        err = np.abs(got - want)
+        rf = np.linalg.norm(got - want) / np.linalg.norm(want)
+        bar = np.maximum(2e-2, bf16_ulp(want))   # bf16 output: no finer than one spacing of its value
+        over = err > bar
+        assert rf <= 5e-3, (step, k, rf)
+        assert np.all(err <= bar + slack), (step, k, float(np.max(err - bar - slack)))
+        assert over.sum() <= max(2, MAX_FRAC_OVER * err.size), (step, k, int(over.sum()))
+        # residual add on the oracle's fp32 stream and attention output: fp32
+        # accumulation over K terms is within gamma_K * sum |terms| (recursive
+        # summation bound, gamma_K = K u / (1 - K u), u = 2^-24), plus the
+        # fp32 roundings of the incoming stream and of the result
+        x32 = torch.from_numpy(ref["xs"][k].astype(np.float32)).cuda()
+        xb = torch.empty((B, C, D), dtype=torch.bfloat16, device="cuda")
+        run.residual(k, to_bf16(want, (B, C, -1)), x32, xb)
+        nxt = ref["xs"][k + 1]
+        o = want.reshape(R, -1)
+        Wo = run_wo[k]
+        bound = gamma(o.shape[1]) * (np.abs(o) @ np.abs(Wo).T) + U * (np.abs(ref["xs"][k]) + np.abs(nxt))
+        rerr = np.abs(x32.cpu().numpy().astype(np.float64) - nxt)
+        assert np.all(rerr <= bound), (step, k, float(np.max(rerr - bound)))
+        report.append((k, float(err.max()), rf, int(over.sum())))
+    # tied LM head on the oracle's final stream
+    # (bf16 result: one ulp of rounding plus the fp32 accumulation bound,
+    # which dominates where the terms cancel)
+    logits = run.head(to_bf16(ref["x"], (B, C, D)))
+    got = logits.float().cpu().numpy()[rows].astype(np.float64)
+    want = ref["logits"][rows]
+    bound = bf16_ulp(want) + gamma(D) * (np.abs(ref["x"][rows]) @ np.abs(E_exact).T)
+    assert np.all(np.abs(got - want) <= bound), float(np.max(np.abs(got - want) - bound))
+    # sampler on the head's logits
+    dev = "cuda"
+    fr = torch.from_numpy((np.zeros(R) if frozen is None else frozen).astype(np.uint8)).to(dev)
+    ft = torch.from_numpy((np.zeros(R) if ftok is None else ftok).astype(np.int32)).to(dev)
+    run.sample(logits, step, fr, ft)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    H = ref["entropy"]
+    ent = run.entropy.cpu().numpy().astype(np.float64)[rows]
+    assert np.max(np.abs(ent - H)) <= 1e-3, (step, float(np.max(np.abs(ent - H))))
+    ok = np.abs(H - cfg.bound) > TIE
+    np.testing.assert_array_equal(run.mask.cpu().numpy()[rows][ok], ref["commit_mask"][ok])
+    np.testing.assert_array_equal(run.next_tokens.cpu().numpy()[rows][ok], ref["tokens"][ok])
+    soft = run.soft.cpu().numpy().astype(np.float64)[rows]
+    rf = np.linalg.norm(soft - ref["soft_emb"]) / np.linalg.norm(ref["soft_emb"])
+    assert rf <= 5e-3, (step, rf)
+    print(f"step {step}: layers (k, max|err|, rel-Fro, elements over the bar) {report}; "
+          f"max |dH| {np.max(np.abs(ent - H)):.2e}, soft rel-Fro {rf:.2e}, ties {int((~ok).sum())}")
+    return int(ref["commit_mask"].sum())
+
+
+def test_mini_loop_every_stage_every_step(cv):
+    """2 canvases x 32, prefix 160, 5 sliding (window 48) + 1 global layers,
+    vocab 4096, 4 steps: every stage of every step, all rows."""
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    cfg = wl.mini_loop_config(steps=4)
+    inp = wl.make_loop_inputs(cfg)
+    run = CanvasLoop(inp)
+    layers = oracle_layers(inp)
+    E = wl.as_f64(inp.E, "bf16")
+    tokens = inp.tokens0.astype(np.int64)
+    soft, frozen, ftok = None, None, None
+    R = cfg.B * cfg.C
+    commits = []
+    for s in range(cfg.steps):
+        ref = oloop.loop_step(layers, E, tokens, soft, s, cfg.B, cfg.C, cfg.seed, cfg.bound, frozen, ftok,
+                              slack_eps=SLACK_EPS)
+        commits.append(check_step(cv, run, ref, cfg, s, frozen, ftok, np.arange(R), [L["W_o"] for L in layers], E))
+        tokens, soft = ref["tokens"], ref["soft_emb"]
+        frozen, ftok = ref["commit_mask"], ref["tokens"]
+    assert 0 < commits[-1] < R     # both branches of the sampler are exercised
+    assert commits == sorted(commits)
+
+
+def test_loop_workload_first_step_every_stage(cv):
+    """4 canvases x 256, prefix 1024, 5 sliding + 1 global layers (the sliding-
+    and global-layer shapes), vocab 262144: every stage of step 0, all rows of
+    every layer, a sample of sampler rows."""
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    cfg = wl.loop_config(1024, steps=1)
+    inp = wl.make_loop_inputs(cfg)
+    run = CanvasLoop(inp)
+    rows = np.array([0, 1, 255, 256, 600, 777, 1022, 1023])
+    layers = oracle_layers(inp)
+    E = wl.as_f64(inp.E, "bf16")
+    ref = oloop.loop_step(layers, E, inp.tokens0, None, 0, cfg.B, cfg.C, cfg.seed, cfg.bound, sample_rows=rows,
+                          slack_eps=SLACK_EPS)
+    check_step(cv, run, ref, cfg, 0, None, None, rows, [L["W_o"] for L in layers], E)
+
+
+def _free_run_invariants(cfg, run, steps):
+    R = cfg.B * cfg.C
+    prev_mask = np.zeros(R, np.uint8)
+    prev_tok = None
+    for s in range(steps):
+        run.step()
+        mask = run.mask.cpu().numpy()
+        tok = run.tokens.cpu().numpy()
+        H = run.entropy.cpu().numpy()
+        amax = run.argmax.cpu().numpy()
+        assert np.all(H >= -1e-6) and np.all(H <= np.log(cfg.V) + 1e-3)
+        assert np.all(mask[prev_mask == 1] == 1)                      # committed positions stay committed
+        if prev_tok is not None:
+            np.testing.assert_array_equal(tok[prev_mask == 1], prev_tok[prev_mask == 1])
+        new = (mask == 1) & (prev_mask == 0)
+        np.testing.assert_array_equal(mask[prev_mask == 0], (H[prev_mask == 0] < cfg.bound).astype(np.uint8))
+        np.testing.assert_array_equal(tok[new], amax[new])            # newly committed: the argmax
+        ren = np.nonzero(mask == 0)[0]
+        want = np.array([splitmix.renoise_token(cfg.seed, s, int(r), cfg.V) for r in ren], dtype=np.int64)
+        np.testing.assert_array_equal(tok[ren], want)                 # the rest: the renoise draw
+        prev_mask, prev_tok = mask, tok
+    return int(prev_mask.sum())
+
+
+def test_mini_loop_free_run_invariants(cv):
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    cfg = wl.mini_loop_config(steps=8)
+    run = CanvasLoop(wl.make_loop_inputs(cfg))
+    committed = _free_run_invariants(cfg, run, cfg.steps)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    assert committed > 0
+
+
+def test_loop_workload_48_steps_invariants(cv):
+    """48 steps at prefix 1024 on the full loop; with these weights the
+    distributions stay near-uniform, so every position is renoised every step."""
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    cfg = wl.loop_config(1024, steps=48)
+    run = CanvasLoop(wl.make_loop_inputs(cfg))
+    committed = _free_run_invariants(cfg, run, cfg.steps)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    assert committed == 0
