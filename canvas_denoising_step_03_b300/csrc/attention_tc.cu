@@ -16,7 +16,7 @@
 // prefix in place (paged cache through the block table, or the dense global
 // keys) or from the dense tail buffers.
 //
-// Roles (192 threads):
+// Roles (320 threads):
 //   warp 0       TMA producer: Q tile once; then K chunks and V sub-blocks in
 //                the order the MMA warp consumes them, through a ring of
 //                32 KB stages (128-byte swizzle).
@@ -25,9 +25,11 @@
 //                into one of two S buffers; O += P_n V_n (M=128, N=DV, P read
 //                from TMEM where the softmax wrote it over S_n, V from shared
 //                memory, MN-major).  Issue order QK0 QK1 PV0 QK2 PV1 ...
-//   warps 2..5   softmax and epilogue, one query row per thread (TMEM lane):
-//                S from TMEM, masking, running max in the log2 domain,
-//                P = 2^(S c - m) rounded to bf16 and stored back to TMEM.
+//   warps 2..9   softmax and epilogue, one query row per thread (TMEM lane)
+//                and one 64-key half of each block per warp: S from TMEM,
+//                masking, running max in the log2 domain (agreed between the
+//                two warps of a row), P = 2^(S c - m) rounded to bf16 and
+//                stored back to TMEM.
 //                The accumulator is rescaled only when the running max grows
 //                by more than 8 (P stays below 2^8), so most blocks never
 //                touch O.
@@ -44,10 +46,15 @@ namespace canvas {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // TMA warp, MMA warp, 8 softmax / epilogue warps
 constexpr int kStageBytes = 32768;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
+// exchange area of the two softmax warps of a row quadrant: the block maxima
+// of the two key halves as bf16 rounded up ([2 blocks][2 halves][128 rows]),
+// then the final partial sums (fp32 [2 halves][128 rows])
+constexpr int kXchgBytes = 1024;
+constexpr int kBarBytes = 256;  // 18 mbarriers, the TMEM address and the abort flag
 
 template <int D>
 struct Cfg {
@@ -57,8 +64,20 @@ struct Cfg {
   static constexpr int KST = NCH / KCH;          // K stages per block
   static constexpr int NST = D == 512 ? 3 : 5;   // ring stages
   static constexpr int QBytes = NCH * 16384;
-  static constexpr int Smem = QBytes + NST * kStageBytes + 1024 + 256;
+  static constexpr int Smem = QBytes + NST * kStageBytes + 1024 + kBarBytes + kXchgBytes;
 };
+
+// bf16 bit pattern of the smallest bf16 value >= x (x finite or -inf).
+__device__ __forceinline__ uint16_t bf16_bits_up(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0xffffu) != 0u && (u & 0x7f800000u) != 0x7f800000u) {
+    // drop the low bits towards zero, then step away from zero for positive
+    // values (towards +inf); negative values truncated are already larger
+    u &= 0xffff0000u;
+    if (!(u >> 31)) u += 0x10000u;
+  }
+  return uint16_t(u >> 16);
+}
 
 // The block sequence of one CTA (identical in every thread).
 struct Seq {
@@ -128,8 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;   // [2]
   uint64_t* pv_done = p_full + 2;  // [2]
   uint64_t* drain = pv_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xbar = drain + 1;      // [4] the two softmax warps of a row quadrant
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
+  static_assert((2 * K::NST + 1 + 2 * 3 + 1 + 4) * 8 + 8 <= kBarBytes, "barrier area");
+  uint16_t* xmax = reinterpret_cast<uint16_t*>(ring + K::NST * kStageBytes + kBarBytes);  // [2][2][128]
+  float* xsum = reinterpret_cast<float*>(xmax);                                          // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int x = blockIdx.x;
@@ -157,10 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&s_full[j], 1);
-      mbar_init(&p_full[j], 4);  // one arrival per softmax warp
+      mbar_init(&p_full[j], 8);  // one arrival per softmax warp
       mbar_init(&pv_done[j], 1);
     }
     mbar_init(drain, 1);
+    for (int j = 0; j < 4; ++j) mbar_init(&xbar[j], 2);
     flags[0] = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&maps.q);
@@ -314,7 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------ softmax + epilogue
+    // Eight warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (one query row
+    // per thread) and key half h = (w - 2) / 4 of every block (columns
+    // 64 h .. 64 h + 63, one 64-key sub-block).  The two warps of a row
+    // quadrant agree on the running maximum through shared memory once per
+    // block (named barrier 1 + quadrant), keep their own partial sums, and
+    // split the value columns of O for the rescale and the epilogue.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int lrow = quad * 32 + lane;
     const uint32_t lane_off = uint32_t(quad * 32) << 16;
     const int GC = a.G * a.C;
@@ -322,8 +353,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = R < GC;
     const int g = valid ? R / a.C : 0, i = valid ? R % a.C : 0;
     const int lo_row = valid ? window_lo(a, sq.P, i) : 0;
+    constexpr int DVH = K::DV / 2;  // value columns this warp rescales / writes
     float m_run = -INFINITY, l = 0.f;
     bool alive = true;
+    // the pair of warps of this quadrant meet on xbar[quad] once per block and
+    // twice in the epilogue (phase k completes when both warps arrive);
+    // bounded, so an aborted partner cannot strand a warp
+    int xphase = 0;
+    auto pair_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[quad]);
+      const bool ok = mbar_wait(&xbar[quad], uint32_t(xphase & 1), flags);
+      ++xphase;
+      return ok;
+    };
     for (int n = 0; n < nb; ++n) {
       if (!mbar_wait(&s_full[n & 1], (n >> 1) & 1, flags)) {
         alive = false;
@@ -331,49 +374,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + 256 + (n & 1) * 128;
-      // visibility of the block's 128 keys: a uniform test first, per-key bits otherwise
+      // this warp's 64 keys: sub-block sb of the key sequence
       const int kb = sq.kb0 + n;
-      bool clean = true;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int sb = 2 * kb + u;
-        if (sb < sq.n_pre) {
-          clean = clean && (sq.s0 + 64 * sb >= sq.lo_max);
-        } else {
-          const int t0 = 64 * (sb - sq.n_pre);
-          clean = clean && (t0 + 64 <= sq.T) && (sq.P64 + t0 >= sq.lo_max || sq.P64 + t0 >= sq.P);
-        }
+      const int sb = 2 * kb + half;
+      int pos0, hi_off = 64;
+      if (sb < sq.n_pre) {
+        pos0 = sq.s0 + 64 * sb;
+      } else {
+        const int t0 = 64 * (sb - sq.n_pre);
+        pos0 = sq.P64 + t0;
+        hi_off = min(64, sq.T - t0);
       }
-      // S row of this thread: 128 fp32 values in registers (four TMEM loads in flight)
-      uint32_t sv[kAttnBN];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c4 * 32]));
+      // visible offsets [lo_off, hi_off): position >= the row's window start
+      // (lo_row <= P, so canvas keys pass) and, in the tail, before the padding
+      const int lo_off = max(0, lo_row - pos0);
+      uint32_t sv[64];
+      tmem_ld32(tS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
-      if (!clean) {
-        // within sub-block u the visible keys are the offsets [lo_off, hi_off):
-        // position >= the row's window start (lo_row <= P, so canvas keys pass)
-        // and, in the tail, rows before the zero padding
+      if (__any_sync(0xffffffffu, lo_off > 0 || hi_off < 64)) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int sb = 2 * kb + u;
-          int pos0, hi_off = 64;
-          if (sb < sq.n_pre) {
-            pos0 = sq.s0 + 64 * sb;
-          } else {
-            const int t0 = 64 * (sb - sq.n_pre);
-            pos0 = sq.P64 + t0;
-            hi_off = min(64, sq.T - t0);
-          }
-          const int lo_off = max(0, lo_row - pos0);
-#pragma unroll
-          for (int off = 0; off < 64; ++off)
-            if (off < lo_off || off >= hi_off) sv[u * 64 + off] = __float_as_uint(-INFINITY);
-        }
+        for (int off = 0; off < 64; ++off)
+          if (off < lo_off || off >= hi_off) sv[off] = __float_as_uint(-INFINITY);
       }
-      // block maximum in the log2 domain (c_log2 > 0)
+      // block maximum in the log2 domain (c_log2 > 0), agreed by the pair:
+      // each half publishes its maximum rounded up to bf16, and both take the
+      // larger published value (an upper bound of the block maximum, the same
+      // bits in both warps)
       float smax = __uint_as_float(sv[0]);
 #pragma unroll
-      for (int c = 1; c < kAttnBN; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
+      for (int c = 1; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
+      const uint16_t mine = bf16_bits_up(smax);
+      xmax[((n & 1) * 2 + half) * kAttnBM + lrow] = mine;
+      if (!pair_sync()) {
+        alive = false;
+        break;
+      }
+      const uint16_t other = xmax[((n & 1) * 2 + (half ^ 1)) * kAttnBM + lrow];
+      smax = fmaxf(bf16_bits_to_f32(mine), bf16_bits_to_f32(other));
       const float bmax = smax * a.c_log2;
       const float m_new = fmaxf(m_run, bmax);
       const bool need = (m_run != -INFINITY) && (m_new > m_run + kRescaleLog2);
@@ -385,16 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // P = 2^(s c - m) rounded to bf16 pairs, written over the first 64 columns
-      // of S (keys 32 c4 .. 32 c4 + 31 -> columns 16 c4 .. 16 c4 + 15; the S
-      // values are already in registers)
+      // P = 2^(s c - m) rounded to bf16 pairs over this half's S columns
+      // (keys 64 h + 32 c2 .. -> packed columns 32 h + 16 c2 ..)
       float l_lo = 0.f, l_hi = 0.f;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int c = c4 * 32 + 2 * j;
+          const int c = c2 * 32 + 2 * j;
           const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), a.c_log2, -m_use));
           const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), a.c_log2, -m_use));
           if (a.vs_pre == nullptr) {
@@ -409,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sc[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int ce = c + e, sb = 2 * kb + (ce >> 6), off = ce & 63;
-              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + sq.s0 + 64 * sb + off]
-                                    : a.vs_tail[(size_t)grp * a.Tpad + 64 * (sb - sq.n_pre) + off];
+              const int off = c + e;
+              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + pos0 + off]
+                                    : a.vs_tail[(size_t)grp * a.Tpad + (pos0 - sq.P64) + off];
             }
             pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
             const float w0 = __uint_as_float(pk[j] << 16), w1 = __uint_as_float(pk[j] & 0xffff0000u);
@@ -419,12 +456,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_hi += sc[1] > 0.f ? w1 / sc[1] : 0.f;
           }
         }
-        tmem_st16(tS + c4 * 16, pk);
+        tmem_st16(tS + half * 32 + c2 * 16, pk);
       }
       l += l_lo + l_hi;
-      // rescale O (after P is stored, so the S registers are free): the
-      // previous block's P.V must have landed in O first; P.V of this block
-      // waits for the arrival below
+      // rescale this warp's half of O (after P is stored): the previous
+      // block's P.V must have landed first; P.V of this block waits for the
+      // arrivals below
       if (__any_sync(0xffffffffu, need)) {
         if (!mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) {
           alive = false;
@@ -432,13 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < K::DV / 32; ++cc) {
+        for (int cc = 0; cc < DVH / 32; ++cc) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + cc * 32, r);
+          const uint32_t col = uint32_t(half * DVH + cc * 32);
+          tmem_ld32(tmem + lane_off + col, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(tmem + lane_off + cc * 32, r);
+          tmem_st32(tmem + lane_off + col, r);
         }
       }
       tmem_st_wait();
@@ -450,15 +488,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
       tc_fence_after();
     }
-    // ---------------- epilogue
+    // ---------------- epilogue: the pair's partial sums, then each warp
+    // writes its half of the row's value columns
+    float l_row = l;
+    if (alive) alive = pair_sync();  // both warps are past their last read of the maxima
+    if (alive) {
+      xsum[half * kAttnBM + lrow] = l;
+      alive = pair_sync();
+      l_row = l + xsum[(half ^ 1) * kAttnBM + lrow];
+    }
     if (alive) {
       const int h = hk * a.G + g;
       if (a.nsplit == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d + dvp * K::DV;
-        for (int cc = 0; cc < K::DV / 32; ++cc) {
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d + dvp * K::DV + half * DVH;
+        for (int cc = 0; cc < DVH / 32; ++cc) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + cc * 32, r);
+          tmem_ld32(tmem + lane_off + uint32_t(half * DVH + cc * 32), r);
           tmem_ld_wait();
           if (valid) {
             uint32_t pk[16];
@@ -470,15 +516,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
-        if (valid && dvp == 0 && a.lse != nullptr)
-          a.lse[((size_t)b * a.C + i) * a.Hq + h] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+        if (valid && dvp == 0 && half == 0 && a.lse != nullptr)
+          a.lse[((size_t)b * a.C + i) * a.Hq + h] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
       } else {
         const size_t prow = ((size_t)split * a.B * a.Hkv + grp) * (size_t)(a.q_tiles * kAttnBM) + qt * kAttnBM + lrow;
-        float* dst = a.part_o + prow * a.d + dvp * K::DV;
-        for (int cc = 0; cc < K::DV / 32; ++cc) {
+        float* dst = a.part_o + prow * a.d + dvp * K::DV + half * DVH;
+        for (int cc = 0; cc < DVH / 32; ++cc) {
           uint32_t r[32];
           if (nb >= 1) {
-            tmem_ld32(tmem + lane_off + cc * 32, r);
+            tmem_ld32(tmem + lane_off + uint32_t(half * DVH + cc * 32), r);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -490,9 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             o4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
                                 __uint_as_float(r[4 * j + 3]));
         }
-        if (dvp == 0) {
+        if (dvp == 0 && half == 0) {
           a.part_ml[prow * 2] = m_run;
-          a.part_ml[prow * 2 + 1] = l;
+          a.part_ml[prow * 2 + 1] = l_row;
         }
       }
     }

@@ -92,11 +92,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
 
 // Wait for the phase of parity `parity` of `bar` to complete.  Gives up when
 // *abort is set by another thread of the CTA, or after the timeout, in which
-// case it sets *abort, records CANVAS_ERR_TIMEOUT and returns false.
+// case it sets *abort, records CANVAS_ERR_TIMEOUT and returns false.  The
+// first probe is inline; the polling loop is a separate function, so its
+// register saves stay off the path where the phase is already complete.
 template <bool kCluster = false>
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const uint32_t a = smem_u32(bar);
-  if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
@@ -109,6 +110,13 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile 
       }
     }
   }
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t a = smem_u32(bar);
+  if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  return mbar_wait_slow<kCluster>(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------------------
