@@ -529,6 +529,10 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     t.window = global ? 0 : window;
     t.Tpad = pl.Tpad;
     t.kpre_paged = global ? 0 : 1;
+    // 2-SM MMAs halve the K / V bytes each SM receives per key block; that
+    // pays where those bytes bound the kernel (head_dim 512: 439 -> 377 us on
+    // the global-layer workload), not at head_dim 256 (166 -> 178 us)
+    t.pair = d == 512 ? 1 : 0;
     t.block_table = kv->block_table;
     t.max_pages = kv->max_pages_per_seq;
     t.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;

@@ -139,6 +139,7 @@ constexpr int kAttnBN = 128;       // keys per block
 struct AttnTcArgs {
   int B, C, Hq, Hkv, G, d, DV, dv_parts, q_tiles, nsplit, max_prefix, window, Tpad;
   int kpre_paged;            // 1: prefix keys from the paged pool; 0: dense Kt
+  int pair;                  // 1: 2-SM kernel (CTA pairs share each MMA), head_dim 256 / 512
   const int32_t* block_table;
   int max_pages, page_tokens, num_pages;
   const int32_t* prefix_len;
