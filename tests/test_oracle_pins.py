@@ -458,3 +458,109 @@ def test_row_slack_bounds_brute_force_flips(which):
         worst = np.maximum(worst, np.abs(out(qq, kk, vv) - base))
     assert np.all(worst <= bound + 1e-15), (worst, bound)
     assert np.all(bound <= 50 * worst + 1e-12)
+
+
+# ---------------------------------------------------------------- the loop step
+def _tiny_loop(seed=5):
+    """Two layers (sliding with a window, global with W_v = W_k), D != Hq*d
+    so that a transposed W_o cannot pass."""
+    rng = np.random.default_rng(seed)
+    B, C, D, P, V = 2, 3, 6, 5, 16
+    Hq, Hkv, d = 2, 1, 4
+    layers = []
+    for k, (kind, window) in enumerate((("sliding", 2), ("global", 0))):
+        L = dict(W_q=onum.bf16_round(rng.normal(size=(Hq * d, D)) / 2),
+                 W_k=onum.bf16_round(rng.normal(size=(Hkv * d, D)) / 2),
+                 W_v=onum.bf16_round(rng.normal(size=(Hkv * d, D)) / 2) if kind == "sliding" else None,
+                 W_o=onum.bf16_round(rng.normal(size=(D, Hq * d))),
+                 gamma_q=np.full(d, 1.1), gamma_k=np.full(d, 0.7), freq=onum.rope_frequencies(d, 1e4),
+                 eps=1e-6, Hq=Hq, Hkv=Hkv, d=d, layer=kind, window=window, prefix=P,
+                 cache_k=onum.bf16_round(rng.normal(size=(B, Hkv, P, d))),
+                 cache_v=onum.bf16_round(rng.normal(size=(B, Hkv, P, d))) if kind == "sliding" else None)
+        layers.append(L)
+    E = onum.bf16_round(rng.normal(size=(V, D)))
+    tokens = rng.integers(0, V, size=B * C)
+    soft_prev = rng.normal(size=(B * C, D)) * 0.1
+    return layers, E, tokens, soft_prev, B, C, D, V
+
+
+def test_loop_step_glue_brute_force():
+    """oracle.loop.loop_step against the step written out element by element:
+    input = E[token] + soft_emb of the previous step; per layer the residual
+    gains bf16(attention) times W_o^T; logits = bf16(bf16(x) E^T); the
+    sampler's commit / renoise rule with each row's own index; soft_emb =
+    bf16(p) E.  The attention layer itself is the oracle's (pinned above)."""
+    from oracle import loop as oloop
+    layers, E, tokens, soft_prev, B, C, D, V = _tiny_loop()
+    R = B * C
+    step, seed = 3, 9
+    # residual stream and logits by explicit loops
+    x = np.zeros((R, D))
+    for r in range(R):
+        for j in range(D):
+            x[r, j] = E[tokens[r], j] + soft_prev[r, j]
+    xs = [x.copy()]
+    attn = []
+    for L in layers:
+        out = oatt.canvas_attention(onum.bf16_round(x).reshape(B, C, D), L["W_q"], L["W_k"], L["W_v"], L["Hq"],
+                                    L["Hkv"], L["d"], L["gamma_q"], L["gamma_k"], L["eps"], L["freq"], L["layer"],
+                                    L["cache_k"], L["cache_v"], np.full(B, L["prefix"]), L["window"],
+                                    storage="bf16")[0]
+        ob = onum.bf16_round(out).reshape(R, -1)
+        attn.append(ob)
+        nxt = x.copy()
+        for r in range(R):
+            for j in range(D):
+                nxt[r, j] += sum(ob[r, c] * L["W_o"][j, c] for c in range(ob.shape[1]))
+        x = nxt
+        xs.append(x.copy())
+    xb = onum.bf16_round(x)
+    logits = np.zeros((R, V))
+    for r in range(R):
+        for v in range(V):
+            logits[r, v] = sum(xb[r, j] * E[v, j] for j in range(D))
+    logits = onum.bf16_round(logits)
+    H = np.array([-sum(p * math.log(p) for p in np.exp(lg - lg.max()) / np.exp(lg - lg.max()).sum() if p > 0)
+                  for lg in logits])
+    bound = float(np.median(H))   # both branches of the rule
+    ref = oloop.loop_step(layers, E, tokens, soft_prev, step, B, C, seed, bound)
+    for k in range(len(layers) + 1):
+        np.testing.assert_allclose(ref["xs"][k], xs[k], rtol=1e-12, atol=1e-12)
+    for k in range(len(layers)):
+        np.testing.assert_array_equal(ref["attn"][k].reshape(R, -1), attn[k])
+    np.testing.assert_array_equal(ref["logits"], logits)
+    np.testing.assert_allclose(ref["entropy"], H, rtol=1e-10)
+    committed = 0
+    for r in range(R):
+        if H[r] < bound:
+            committed += 1
+            assert ref["commit_mask"][r] == 1 and ref["tokens"][r] == int(np.argmax(logits[r]))
+        else:
+            assert ref["commit_mask"][r] == 0
+            assert ref["tokens"][r] == osm.renoise_token(seed, step, r, V)
+        p = onum.bf16_round(np.exp(logits[r] - logits[r].max()) / np.exp(logits[r] - logits[r].max()).sum())
+        want = [sum(p[v] * E[v, j] for v in range(V)) for j in range(D)]
+        np.testing.assert_allclose(ref["soft_emb"][r], want, rtol=1e-12, atol=1e-14)
+    assert 0 < committed < R
+
+
+def test_loop_step_row_subset_keeps_global_row_keys():
+    """Evaluating the sampler on a subset of rows gives those rows' full-step
+    results, including renoise draws keyed by the global row index; frozen rows
+    keep their tokens."""
+    from oracle import loop as oloop
+    layers, E, tokens, soft_prev, B, C, D, V = _tiny_loop(seed=8)
+    R = B * C
+    frozen = np.zeros(R, np.uint8)
+    frozen[[1, 4]] = 1
+    ftok = np.arange(R) + 3
+    full = oloop.loop_step(layers, E, tokens, soft_prev, 2, B, C, 11, 0.5, frozen, ftok)
+    rows = [4, 1, 5]
+    sub = oloop.loop_step(layers, E, tokens, soft_prev, 2, B, C, 11, 0.5, frozen, ftok, sample_rows=rows)
+    sel = sorted(rows)
+    np.testing.assert_array_equal(sub["rows"], sel)
+    for key in ("tokens", "commit_mask"):
+        np.testing.assert_array_equal(sub[key], full[key][sel])
+    np.testing.assert_allclose(sub["entropy"], full["entropy"][sel], rtol=0, atol=0)
+    np.testing.assert_allclose(sub["soft_emb"], full["soft_emb"][sel], rtol=1e-15, atol=0)
+    assert full["tokens"][1] == 4 and full["tokens"][4] == 7 and full["commit_mask"][[1, 4]].all()

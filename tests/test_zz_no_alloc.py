@@ -46,7 +46,7 @@ def _compare(cv, M, N, K, b_layout, accumulate, seed):
 
 
 def test_noalloc_matches_workspace_gemm_twice(cv):
-    # first call: K split across CTAs (the scratch holds partials and tickets);
+    # first call: K split across CTAs (the scratch holds the split partials);
     # second call: another shape and B layout, accumulating into C
     for M, N, K in ((128, 256, 4096), (200, 520, 2048)):
         assert cv.canvas_gemm_workspace_size(M, N, K) <= cv.CANVAS_GEMM_NOALLOC_SCRATCH_BYTES
