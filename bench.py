@@ -9,8 +9,11 @@ bf16).  All inputs are seeded synthetic draws (canvas_workloads); no dataset or
 trained weights are involved.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --workload loop --prefix P [--steps K] [--warmup W]
 
-Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own step on
+Prints ONE JSON line (rank 0).  ``--workload loop`` times instead the batched
+denoising loop (4 canvases x 256, 5 sliding + 1 global layers, vocab 262144,
+committed prefix P), one line per run.  Under torchrun every rank runs its own step on
 its own GPU (canvases are independent: weak scaling, no data-path
 collective); times are the max over ranks.  ``--impl reference`` times the
 fp64 CPU oracle (the reference arm of this tier) on bounded samples.
@@ -130,6 +133,11 @@ class ClockSampler:
                                         stderr=subprocess.DEVNULL)
         except Exception as e:
             self.smi, self.err = None, self.err + "; " + repr(e)
+            return
+        # nvidia-smi takes a moment to start: begin timing once it samples
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.smi_file.name) == 0:
+            time.sleep(0.05)
 
     def _stop_smi(self):
         self.smi.terminate()
@@ -387,6 +395,123 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# --------------------------------------------------------------------------- the batched loop
+def run_loop(args, rank, world, local_rank):
+    """Steps of the batched denoising loop (canvas_denoising_step_03_b300.loop):
+    per step, 6 attention layers + the sampler (the metric's attn+sampler
+    time, from CUDA events around those calls) and the whole step with its
+    glue (embedding, W_o, LM head)."""
+    import torch
+    import torch.distributed as dist
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import canvas_denoising_step_03_b300 as cv
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = wl.loop_config(args.prefix, steps=args.warmup + args.steps)
+    run = CanvasLoop(wl.make_loop_inputs(cfg), device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        run.step()
+    torch.cuda.synchronize()
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    nl = len(run.layers)
+
+    def new_ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+    rec = []
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = cv.canvas_kernel_launches()
+    for k in range(args.steps):
+        marks = []
+        t0 = new_ev()
+        run.step(mark=lambda name: marks.append((name, new_ev())))
+        rec.append((t0, new_ev(), marks))
+    torch.cuda.synchronize()
+    launches = cv.canvas_kernel_launches() - launches0
+    clk = clocks.stop()
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    step_ms, attn_ms, samp_ms, layer_ms = [], [], [], [[] for _ in range(nl)]
+    for t0, t1, marks in rec:
+        step_ms.append(t0.elapsed_time(t1))
+        a = [m for m in marks if m[0].startswith("attention")]
+        per = [a[2 * j][1].elapsed_time(a[2 * j + 1][1]) for j in range(nl)]
+        for j in range(nl):
+            layer_ms[j].append(per[j])
+        attn_ms.append(sum(per))
+        sm = {n: e for n, e in marks if n.startswith("sample")}
+        samp_ms.append(sm["sample_begin"].elapsed_time(sm["sample_end"]))
+    ms_core = statistics.mean(a + s_ for a, s_ in zip(attn_ms, samp_ms))
+    ms_step = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_core, ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_core, ms_step = (float(v) for v in t.tolist())
+    # end to end: the step's result (tokens, commit mask) read back to pinned
+    # host memory inside every timed step
+    tok_h = torch.empty(run.tokens.shape, dtype=run.tokens.dtype).pin_memory()
+    mask_h = torch.empty(run.mask.shape, dtype=run.mask.dtype).pin_memory()
+    e2e = []
+    for k in range(args.steps):
+        t0 = new_ev()
+        run.step()
+        tok_h.copy_(run.tokens, non_blocking=True)
+        mask_h.copy_(run.mask, non_blocking=True)
+        e2e.append((t0, new_ev()))
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return None
+    lcs = cfg.layer_cfgs()
+    flops = [attn_flops(lc) for lc in lcs]
+    layer_mean = [statistics.mean(v) for v in layer_ms]
+    g = nl - 1  # the global layer
+    hbm, bf16, peak_src = measured_peaks()
+    g_tflops = flops[g] / (layer_mean[g] * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(world * 1000.0 / ms_core, 3), "unit": "canvas steps/s (attn+sampler)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_core, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded draws; random weights and caches; no dataset)",
+        "config": {"workload": f"batched loop: B={cfg.B} canvases x C={cfg.C}, committed prefix {cfg.prefix}, "
+                               f"{cfg.n_sliding} sliding (d=256, window 1024) + {cfg.n_global} global (d=512) "
+                               f"layers, D={cfg.D}, V={cfg.V}, tied LM head, self-conditioning input",
+                   "l2": "not flushed: every step reads E (1.48 GB) and 1024 x 262144 logits, far above L2",
+                   "parallelism": f"replicas x{world}"},
+        "loop_steps_per_s": round(world * 1000.0 / ms_step, 3),
+        "loop_ms_per_step": round(ms_step, 4),
+        "attention_ms_per_layer": [round(v, 4) for v in layer_mean],
+        "attention_tflops_per_layer": [round(f / (m * 1e-3) / 1e12, 1) for f, m in zip(flops, layer_mean)],
+        "sampler_ms": round(statistics.mean(samp_ms), 4),
+        "roofline": {"kernel": "global-layer canvas_attention call (projections, key preparation, attention)",
+                     "bound": "tensor", "achieved": round(g_tflops, 2), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(g_tflops / bf16, 4), "traffic": None,
+                     "algorithmic": f"{flops[g]:.4g} FLOP per call (4*d per visible query-key pair per head)",
+                     "peak_source": f"{peak_src}, burst"},
+        "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "loop steps/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": int(tok_h.numel() * 4 + mask_h.numel()),
+                "note": "the loop's inputs are the previous step's device state; tokens and commit mask read back "
+                        "every step"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
+
+
 def load_traffic(kernel: str):
     """dram bytes per launch from the committed ncu summary of this kernel, if any."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -476,10 +601,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="step", choices=["step", "loop"])
+    ap.add_argument("--prefix", type=int, default=1024, help="committed prefix of the loop workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -491,6 +618,8 @@ def main():
         dist.init_process_group(backend=backend)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload == "loop":
+        line = run_loop(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0 and line is not None:

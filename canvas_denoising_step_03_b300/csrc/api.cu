@@ -116,59 +116,134 @@ canvas_status make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, ui
   return CANVAS_OK;
 }
 
+// fp32 [z][rows][cols] (row pitch ld elements, slab pitch rows * ld) for TMA
+// stores of 32 x 32 boxes with the 128-byte swizzle; stores clip at every
+// edge, so no box spills into the next row block or slab.
+canvas_status make_map_f32_store(CUtensorMap* map, void* ptr, uint64_t z, uint64_t rows, uint64_t cols, uint64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0)
+    return fail(CANVAS_ERR_ARG, "output base address must be 16-byte aligned");
+  if ((ld * 4) % 16 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "output row pitch must be a multiple of 16 bytes");
+  cuuint64_t dims[3] = {cols, rows, z};
+  cuuint64_t strides[2] = {ld * 4, rows * ld * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled (store) failed (%d)", int(r));
+  return CANVAS_OK;
+}
+
+// bf16 [z][rows][cols] for TMA stores of 32-row x 64-column boxes (128-byte rows, 128-byte swizzle)
+canvas_status make_map_bf16_store(CUtensorMap* map, void* ptr, uint64_t z, uint64_t rows, uint64_t cols, uint64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0)
+    return fail(CANVAS_ERR_ARG, "output base address must be 16-byte aligned");
+  if ((ld * 2) % 16 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "output row pitch must be a multiple of 16 bytes");
+  cuuint64_t dims[3] = {cols, rows, z};
+  cuuint64_t strides[2] = {ld * 2, rows * ld * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled (bf16 store) failed (%d)", int(r));
+  return CANVAS_OK;
+}
+
 // ------------------------------------------------------------------ GEMM plan
 struct GemmPlan {
   int m_tiles, n_tiles, kblocks, splits, two_acc;
-  size_t partial_bytes;
+  size_t partial_bytes;  // all problems, each slab 256-byte aligned
 };
 
 constexpr int kNumSms = 148;
 
-GemmPlan plan_gemm(int M, int N, int K) {
+// One launch for nprob problems C_p[M, N_p] = A[M, K] op(B_p).
+GemmPlan plan_gemm_group(int M, const int* N, int nprob, int K) {
   GemmPlan p;
   p.two_acc = M > kGemmBM ? 1 : 0;
   p.m_tiles = (M + 255) / 256;
-  p.n_tiles = (N + kGemmBN - 1) / kGemmBN;
+  p.n_tiles = 0;
+  for (int i = 0; i < nprob; ++i) p.n_tiles += (N[i] + kGemmBN - 1) / kGemmBN;
   p.kblocks = (K + kGemmBK - 1) / kGemmBK;
   const int tiles = p.m_tiles * p.n_tiles;
   int s = tiles >= kNumSms ? 1 : kNumSms / tiles;
-  s = std::min(s, std::max(1, p.kblocks / 2));
+  // at least 8 K blocks per split: shorter splits are dominated by the
+  // pipeline fill and by writing their fp32 partial tile
+  s = std::min(s, std::max(1, p.kblocks / 8));
   p.splits = std::max(1, s);
-  p.partial_bytes = p.splits > 1 ? size_t(p.splits) * M * N * sizeof(float) : 0;
+  p.partial_bytes = 0;
+  if (p.splits > 1)
+    for (int i = 0; i < nprob; ++i) p.partial_bytes += align_up(size_t(p.splits) * M * N[i] * sizeof(float));
   return p;
 }
 
+GemmPlan plan_gemm(int M, int N, int K) { return plan_gemm_group(M, &N, 1, K); }
+
 size_t gemm_ws_bytes(const GemmPlan& p) { return align_up(p.partial_bytes); }
 
-// C[M,N] = A[M,K] op(B) on the tensor cores; ws holds the split partials.
-canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C, int M, int N, int K,
-                          int accumulate, void* ws, cudaStream_t stream) {
-  const GemmPlan p = plan_gemm(M, N, K);
-  CUtensorMap tmA, tmB;
-  canvas_status st = make_map_bf16(&tmA, A, M, K, kGemmBM, kGemmBK);
-  if (st != CANVAS_OK) return st;
-  if (b_mn_major)
-    st = make_map_bf16(&tmB, B, K, N, 64, 64);
-  else
-    st = make_map_bf16(&tmB, B, N, K, kGemmBN, kGemmBK);
+// C_p[M, N_p] = A[M, K] op(B_p) (+ C_p) for p < nprob on the tensor cores, in
+// one launch; C fp32, or bf16 with out_bf16 (no accumulate); ws holds the
+// split partials.
+canvas_status run_gemm_group(const void* A, const void* const* B, void* const* C, const int* N, int nprob,
+                             int b_mn_major, int M, int K, int accumulate, int out_bf16, void* ws,
+                             cudaStream_t stream) {
+  if (nprob < 1 || nprob > kGemmMaxProblems) return fail(CANVAS_ERR_ARG, "GEMM: 1 to 3 problems per launch");
+  const GemmPlan p = plan_gemm_group(M, N, nprob, K);
+  GemmTcMaps maps;
+  GemmTcArgs g;
+  canvas_status st = make_map_bf16(&maps.A, A, M, K, kGemmBM, kGemmBK);
   if (st != CANVAS_OK) return st;
   Carver cv(ws);
-  GemmTcArgs g;
-  g.partials = cv.take<float>(p.partial_bytes);
-  g.C = C;
+  g.tile0[0] = 0;
+  for (int i = 0; i < nprob; ++i) {
+    if (b_mn_major)
+      st = make_map_bf16(&maps.B[i], B[i], K, N[i], 64, 64);
+    else
+      st = make_map_bf16(&maps.B[i], B[i], N[i], K, kGemmBN, kGemmBK);
+    if (st != CANVAS_OK) return st;
+    g.partials[i] = p.splits > 1 ? cv.take<float>(size_t(p.splits) * M * N[i] * sizeof(float)) : nullptr;
+    if (p.splits > 1)
+      st = make_map_f32_store(&maps.out[i], g.partials[i], uint64_t(p.splits), uint64_t(M), uint64_t(N[i]),
+                              uint64_t(N[i]));
+    else if (out_bf16)
+      st = make_map_bf16_store(&maps.out[i], C[i], 1, uint64_t(M), uint64_t(N[i]), uint64_t(N[i]));
+    else
+      st = make_map_f32_store(&maps.out[i], C[i], 1, uint64_t(M), uint64_t(N[i]), uint64_t(N[i]));
+    if (st != CANVAS_OK) return st;
+    g.C[i] = C[i];
+    g.N[i] = N[i];
+    g.tile0[i + 1] = g.tile0[i] + (N[i] + kGemmBN - 1) / kGemmBN;
+  }
+  for (int i = nprob; i < kGemmMaxProblems; ++i) {
+    maps.B[i] = maps.B[0];
+    maps.out[i] = maps.out[0];
+    g.C[i] = nullptr;
+    g.partials[i] = nullptr;
+    g.N[i] = 0;
+    g.tile0[i + 1] = g.tile0[i];
+  }
   g.M = M;
-  g.N = N;
   g.K = K;
-  g.ldc = N;
+  g.kblocks = p.kblocks;
+  g.splits = p.splits;
   g.accumulate = accumulate;
+  g.out_bf16 = out_bf16;
   g.b_mn_major = b_mn_major;
   g.two_acc = p.two_acc;
   g.m_tiles = p.m_tiles;
-  g.n_tiles = p.n_tiles;
-  g.splits = p.splits;
-  g.kblocks = p.kblocks;
-  CANVAS_CUDA(launch_gemm_tc(tmA, tmB, g, stream));
+  g.nprob = nprob;
+  CANVAS_CUDA(launch_gemm_tc(maps, g, stream));
   return CANVAS_OK;
+}
+
+canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C, int M, int N, int K,
+                          int accumulate, void* ws, cudaStream_t stream) {
+  void* Cv = C;
+  return run_gemm_group(A, &B, &Cv, &N, 1, b_mn_major, M, K, accumulate, 0, ws, stream);
 }
 
 // ------------------------------------------------------------------ attention layout
@@ -211,7 +286,8 @@ AttnLayout attn_layout(int dtype, int B, int C, int D, int Hq, int Hkv, int d, i
   L.proj_v = global ? 0 : M * Hkv * d * 4;
   L.gemm = 0;
   if (dtype == CANVAS_BF16) {
-    L.gemm = std::max(gemm_ws_bytes(plan_gemm(int(M), Hq * d, D)), gemm_ws_bytes(plan_gemm(int(M), Hkv * d, D)));
+    const int Ns[3] = {Hq * d, Hkv * d, Hkv * d};
+    L.gemm = gemm_ws_bytes(plan_gemm_group(int(M), Ns, global ? 2 : 3, D));
   }
   const size_t BH = size_t(B) * Hkv;
   L.qp = M * Hq * d * es;
@@ -303,9 +379,26 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
   if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: bad shape");
   if (b_layout != 0 && b_layout != 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: b_layout must be 0 or 1");
   if (K % 8 != 0 || N % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16: K and N must be multiples of 8");
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: A, B and C must be 16-byte aligned");
   if (!ws_ok(workspace, ws_bytes, canvas_gemm_workspace_size(M, N, K)))
     return fail(CANVAS_ERR_WORKSPACE, "canvas_gemm_bf16: workspace missing, small or misaligned");
   return run_gemm_tc(A, B, b_layout, C, M, N, K, accumulate, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+canvas_status canvas_gemm_bf16_to_bf16(const void* A, const void* B, int b_layout, void* C, int M, int N, int K,
+                                       void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: null pointer");
+  if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: bad shape");
+  if (b_layout != 0 && b_layout != 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: b_layout must be 0 or 1");
+  if (K % 8 != 0 || N % 8 != 0)
+    return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16_to_bf16: K and N must be multiples of 8");
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: A, B and C must be 16-byte aligned");
+  if (!ws_ok(workspace, ws_bytes, canvas_gemm_workspace_size(M, N, K)))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_gemm_bf16_to_bf16: workspace missing, small or misaligned");
+  void* Cv = C;
+  return run_gemm_group(A, &B, &Cv, &N, 1, b_layout, M, K, 0, 1, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ loop glue
@@ -431,14 +524,12 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
   mark_start(CANVAS_KERNEL_PREP, stream);
   if (bf16) {
-    canvas_status st = run_gemm_tc(x, W_q, 0, proj_q, M, Hq * d, D, 0, gws, stream);
+    // one launch for the two or three products (they share x)
+    const void* Ws[3] = {W_q, W_k, W_v};
+    void* outs[3] = {proj_q, proj_k, proj_v};
+    const int Ns[3] = {Hq * d, Hkv * d, Hkv * d};
+    const canvas_status st = run_gemm_group(x, Ws, outs, Ns, global ? 2 : 3, 0, M, D, 0, 0, gws, stream);
     if (st != CANVAS_OK) return st;
-    st = run_gemm_tc(x, W_k, 0, proj_k, M, Hkv * d, D, 0, gws, stream);
-    if (st != CANVAS_OK) return st;
-    if (!global) {
-      st = run_gemm_tc(x, W_v, 0, proj_v, M, Hkv * d, D, 0, gws, stream);
-      if (st != CANVAS_OK) return st;
-    }
   } else {
     CANVAS_CUDA(launch_gemm_simt(x, W_q, 0, false, proj_q, M, Hq * d, D, 0, stream));
     CANVAS_CUDA(launch_gemm_simt(x, W_k, 0, false, proj_k, M, Hkv * d, D, 0, stream));
@@ -514,6 +605,23 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
       maps.kpre = maps.kx;  // never read: no prefix sub-blocks
       maps.vpre = maps.vx;
     }
+    // the 4-SM kernel (head_dim 512) reads keys in 32-row boxes
+    const bool quad = false;  // d == 512 once validated
+    if (quad) {
+      st = make_map_bf16(&maps.kx32, Kx, BH * pl.Tpad, d, 32, 64);
+      if (st != CANVAS_OK) return st;
+      if (max_prefix > 0) {
+        const uint64_t pool_rows = uint64_t(kv->num_pages) * Hkv * kv->page_tokens;
+        st = global ? make_map_bf16(&maps.kpre32, Kt, BH * max_prefix, d, 32, 64)
+                    : make_map_bf16(&maps.kpre32, kv->k_pool, pool_rows, d, 32, 64);
+        if (st != CANVAS_OK) return st;
+      } else {
+        maps.kpre32 = maps.kx32;
+      }
+    } else {
+      maps.kx32 = maps.kx;  // not read by the other kernels
+      maps.kpre32 = maps.kpre;
+    }
     AttnTcArgs t;
     t.B = B;
     t.C = C;
@@ -529,10 +637,11 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     t.window = global ? 0 : window;
     t.Tpad = pl.Tpad;
     t.kpre_paged = global ? 0 : 1;
-    // 2-SM MMAs halve the K / V bytes each SM receives per key block; that
-    // pays where those bytes bound the kernel (head_dim 512: 439 -> 377 us on
-    // the global-layer workload), not at head_dim 256 (166 -> 178 us)
-    t.pair = d == 512 ? 1 : 0;
+    // head_dim 512: four SMs per 256 query rows (two 2-SM pairs split each
+    // key block, so no S is formed twice); 2-SM MMAs do not pay at head_dim
+    // 256 (166 -> 178 us), where one SM per tile stays
+    t.pair = quad ? 2 : 0;
+    t.Qp = static_cast<const __nv_bfloat16*>(Qp);
     t.block_table = kv->block_table;
     t.max_pages = kv->max_pages_per_seq;
     t.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;

@@ -770,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (alive && nb >= 1) qk(0);
       if (alive && nb >= 2) qk(1);
       for (int n = 0; n < nb && alive; ++n) {
-        if (!mbar_wait<true>(&p_full[n & 1], (n >> 1) & 1, flags)) break;
+        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, flags)) break;
         tc_fence_after();
         pv(n);
         if (n + 2 < nb) qk(n + 2);
@@ -973,6 +973,474 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 512 on four SMs: a cluster of two CTA pairs, no duplicated MMA work.
+//
+// The cluster owns 256 query rows (CTA h of each pair: rows 128 h .. 128 h +
+// 127).  Pair p forms S only for key half p of every 128-key block (64 keys,
+// M = 256 MMAs issued by the pair's leader, rank 2 p) and accumulates only
+// value half p of O (256 columns).  The CTAs with the same rows in the two
+// pairs (ranks r and r ^ 2) agree on each block's row maximum by swapping
+// their half maxima, and each sends its bf16 P to the other with st.async
+// into shared memory, so both pairs form O over all 128 keys:
+//   O_p += P_own V[own keys, half p]   (P from TMEM, where the softmax wrote it)
+//        + P_other V[other keys, half p]  (P from shared memory).
+// Half of Q (d 0..255) sits in TMEM, the other half in shared memory, which
+// leaves room for a four-stage ring (two blocks of K and V in flight).
+// TMEM columns: O [0, 256), S / P [256, 320) and [320, 384), Q [384, 512).
+struct Cfg4 {
+  static constexpr int NST = 4;
+  static constexpr int QSBytes = 4 * 16384;  // Q d 256..511: four 64-wide chunks of 128 rows
+  static constexpr int POBytes = 16384;      // the partner's P: 128 rows x 64 keys bf16
+  static constexpr int Smem = QSBytes + 2 * POBytes + NST * kStageBytes + 1024 + kBarBytes + 1024;
+};
+constexpr int kThreads4 = 192;  // TMA warp, MMA warp, 4 softmax / epilogue warps
+
+__global__ void __launch_bounds__(kThreads4, 1)
+    attention_tc4_kernel(const __grid_constant__ AttnTcMaps maps, AttnTcArgs a) {
+  using K = Cfg4;
+  constexpr int D = 512;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sPO = smem + K::QSBytes;  // [2] partner's P
+  uint8_t* ring = sPO + 2 * K::POBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + K::NST * kStageBytes);
+  uint64_t* empty = full + K::NST;
+  uint64_t* q_full = empty + K::NST;
+  uint64_t* qt_ready = q_full + 1;
+  uint64_t* s_full = qt_ready + 1;  // [2]
+  uint64_t* p_full = s_full + 2;    // [2] (pair leader)
+  uint64_t* pv_done = p_full + 2;   // [2] both pairs' P.V of a block
+  uint64_t* mx_full = pv_done + 2;  // [2] the partner's maxima (and, last, its sums)
+  uint64_t* po_full = mx_full + 2;  // [2] the partner's P
+  uint64_t* drain = po_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
+  static_assert((2 * K::NST + 2 + 2 * 5 + 1) * 8 + 8 <= kBarBytes, "barrier area");
+  uint32_t* xin = reinterpret_cast<uint32_t*>(ring + K::NST * kStageBytes + kBarBytes);  // [2][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pp = int(rank >> 1), h = int(rank & 1);
+  const bool leader = h == 0;
+  const uint32_t lead_rank = rank & 2u, partner = rank ^ 2u;
+  const uint16_t pair_mask = uint16_t(3u << lead_rank);
+  int x = blockIdx.x >> 2;
+  const int q_pairs = (a.q_tiles + 1) / 2;
+  const int qp = x % q_pairs;
+  x /= q_pairs;
+  const int split = x % a.nsplit;
+  x /= a.nsplit;
+  const int hk = x % a.Hkv;
+  const int b = x / a.Hkv;
+  const int grp = b * a.Hkv + hk;
+  const int qt = 2 * qp + h;
+  const Seq sq = make_seq(a, b, qp, split, 2 * kAttnBM);
+  if (!sq.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(CANVAS_ERR_BOUNDS);
+    return;  // uniform over the cluster: before any barrier or TMEM allocation
+  }
+  const int nb = sq.nb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < K::NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(qt_ready, 8);  // the softmax warps of both CTAs of the pair
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&p_full[j], 8);
+      mbar_init(&pv_done[j], 2);  // one commit from each pair's leader
+      mbar_init(&mx_full[j], 1);
+      mbar_init(&po_full[j], 1);
+    }
+    mbar_init(drain, 1);
+    flags[0] = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&maps.q);
+    tma_prefetch_desc(&maps.kpre32);
+    tma_prefetch_desc(&maps.vpre);
+    tma_prefetch_desc(&maps.kx32);
+    tma_prefetch_desc(&maps.vx);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of all four CTAs initialised, TMEM allocated in both pairs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t kColS = 256, kColQ = 384;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (every CTA)
+      const uint32_t lead_q = mapa_shared(smem_u32(q_full), lead_rank);
+      if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QSBytes));
+      const int qrow = grp * a.G * a.C + qt * kAttnBM;
+      for (int c = 0; c < 4; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, (4 + c) * 64, qrow);
+      int it = 0;
+      bool alive = true;
+      auto acquire = [&]() -> uint8_t* {
+        const int s = it % K::NST;
+        if (!mbar_wait(&empty[s], ((it / K::NST) & 1) ^ 1, flags)) {
+          alive = false;
+          return nullptr;
+        }
+        if (leader) mbar_arrive_expect_tx(&full[s], uint32_t(2 * kStageBytes));
+        ++it;
+        return ring + s * kStageBytes;
+      };
+      auto lead_full = [&]() { return mapa_shared(smem_u32(&full[(it - 1) % K::NST]), lead_rank); };
+      auto row_of = [&](int sb, bool key, const CUtensorMap*& map) -> int {
+        if (sb < sq.n_pre) {
+          const int pos = sq.s0 + 64 * sb;
+          map = key ? &maps.kpre32 : &maps.vpre;
+          return (key && !a.kpre_paged) ? grp * a.max_prefix + pos : paged_row(a, b, hk, pos);
+        }
+        map = key ? &maps.kx32 : &maps.vx;
+        return grp * a.Tpad + 64 * (sb - sq.n_pre);
+      };
+      auto load_k = [&](int n) {
+        // this CTA's 32 keys of the pair's key half, all of d: 8 chunks of 4 KB
+        uint8_t* dst = acquire();
+        if (!dst) return;
+        const CUtensorMap* map;
+        const int row = row_of(2 * (sq.kb0 + n) + pp, true, map) + 32 * h;
+        const uint32_t bar = lead_full();
+        for (int c = 0; c < 8; ++c) tma_load_2d_pair(dst + c * 4096, map, bar, c * 64, row);
+      };
+      auto load_v = [&](int n) {
+        // all 128 keys of block n, this CTA's 128 columns of value half pp
+        if (!alive) return;
+        uint8_t* dst = acquire();
+        if (!dst) return;
+        const uint32_t bar = lead_full();
+        for (int u = 0; u < 2; ++u) {
+          const CUtensorMap* map;
+          const int row = row_of(2 * (sq.kb0 + n) + u, false, map);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, pp * 256 + h * 128 + c * 64, row);
+        }
+      };
+      for (int n = 0; n < nb && alive; ++n) {
+        load_k(n);
+        if (n >= 1) load_v(n - 1);
+      }
+      if (nb >= 1 && alive) load_v(nb - 1);
+      if (leader) {
+        volatile int no_abort = 0;
+        mbar_wait(q_full, 0, &no_abort);
+        for (int j = max(0, it - K::NST); j < it; ++j) mbar_wait(&full[j % K::NST], (j / K::NST) & 1, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (pair leader)
+      const uint32_t idesc_qk = idesc_bf16_f32(256, 64, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(256, 256, 0, 1);
+      const uint32_t q_base = smem_u32(sQ);
+      int it = 0;
+      bool alive = mbar_wait(q_full, 0, flags) && mbar_wait(qt_ready, 0, flags);
+      tc_fence_after();
+      auto consume = [&]() -> uint32_t {
+        const int s = it % K::NST;
+        if (!mbar_wait(&full[s], (it / K::NST) & 1, flags)) {
+          alive = false;
+          return 0;
+        }
+        tc_fence_after();
+        ++it;
+        return smem_u32(ring + s * kStageBytes);
+      };
+      auto qk = [&](int n) {
+        const uint32_t tS = tmem + kColS + (n & 1) * 64;
+        const uint32_t st = consume();
+        if (!alive) return;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = smem_desc_sw128(st + ch * 4096 + kk * 32, 16, 1024);
+            const uint32_t acc = (ch | kk) != 0 ? 1u : 0u;
+            if (ch < 4) {
+              mma2_bf16_ts(tS, tmem + kColQ + ch * 32 + kk * 8, bd, idesc_qk, acc);
+            } else {
+              const uint64_t ad = smem_desc_sw128(q_base + (ch - 4) * 16384 + kk * 32, 16, 1024);
+              mma2_bf16_ss(tS, ad, bd, idesc_qk, acc);
+            }
+          }
+        }
+        mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
+        mma2_commit_mc(&s_full[n & 1], pair_mask);
+      };
+      auto pv = [&](int n) {
+        const uint32_t tS = tmem + kColS + (n & 1) * 64;
+        const uint32_t st = consume();
+        if (!alive) return;
+        const uint32_t po = smem_u32(sPO + (n & 1) * K::POBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = smem_desc_sw128(st + pp * 8192 + kk * 2048, 16384, 1024);
+          mma2_bf16_ts(tmem, tS + kk * 8, bd, idesc_pv, (n | kk) != 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = smem_desc_sw128(po + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(st + (1 - pp) * 8192 + kk * 2048, 16384, 1024);
+          mma2_bf16_ss(tmem, ad, bd, idesc_pv, 1u);
+        }
+        mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
+        mma2_commit_mc(&pv_done[n & 1], 0xF);
+      };
+      if (alive && nb >= 1) qk(0);
+      if (alive && nb >= 2) qk(1);
+      for (int n = 0; n < nb && alive; ++n) {
+        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, flags)) break;
+        tc_fence_after();
+        pv(n);
+        if (n + 2 < nb) qk(n + 2);
+      }
+      // every MMA has completed in both CTAs of the pair before either releases TMEM
+      mma2_commit_mc(drain, pair_mask);
+    }
+    if (lane == 0) {
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue (every CTA)
+    const int quad = warp & 3;
+    const int lrow = quad * 32 + lane;
+    const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    const int GC = a.G * a.C;
+    const int R = qt * kAttnBM + lrow;
+    const bool valid = R < GC;
+    const int g = valid ? R / a.C : 0, i = valid ? R % a.C : 0;
+    const int lo_row = valid ? window_lo(a, sq.P, i) : 0;
+    const bool counter = warp == 2 && lane == 0;  // posts this CTA's expected exchange bytes
+    // remote addresses; the second barrier of each pair sits 8 bytes after the first
+    const uint32_t lead_p0 = mapa_shared(smem_u32(&p_full[0]), lead_rank);
+    const uint32_t peer_mx0 = mapa_shared(smem_u32(&mx_full[0]), partner);
+    const uint32_t peer_po0 = mapa_shared(smem_u32(&po_full[0]), partner);
+    const uint32_t peer_xin = mapa_shared(smem_u32(xin), partner);
+    const uint32_t peer_sPO = mapa_shared(smem_u32(sPO), partner);
+    // Q d 0..255 of this row into TMEM (zeros past the last row of the group)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(a.Qp + ((size_t)grp * GC + (valid ? R : 0)) * D);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 u = valid ? src[ch * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * j] = u.x;
+          w[4 * j + 1] = u.y;
+          w[4 * j + 2] = u.z;
+          w[4 * j + 3] = u.w;
+        }
+        tmem_st32(tmem + lane_off + kColQ + ch * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(qt_ready), lead_rank));
+    }
+    float m_run = -INFINITY, l = 0.f;
+    bool alive = true;
+    for (int n = 0; n < nb; ++n) {
+      const int buf = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
+      if (counter) {
+        mbar_arrive_expect_tx(&mx_full[buf], 4u * kAttnBM);
+        mbar_arrive_expect_tx(&po_full[buf], uint32_t(K::POBytes));
+      }
+      if (!mbar_wait(&s_full[buf], ph, flags)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + kColS + buf * 64;
+      const int sb = 2 * (sq.kb0 + n) + pp;
+      int pos0, hi_off = 64;
+      if (sb < sq.n_pre) {
+        pos0 = sq.s0 + 64 * sb;
+      } else {
+        const int t0 = 64 * (sb - sq.n_pre);
+        pos0 = sq.P64 + t0;
+        hi_off = min(64, sq.T - t0);
+      }
+      const int lo_off = max(0, lo_row - pos0);
+      uint32_t sv[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_wait();
+      if (__any_sync(0xffffffffu, lo_off > 0 || hi_off < 64)) {
+#pragma unroll
+        for (int off = 0; off < 64; ++off)
+          if (off < lo_off || off >= hi_off) sv[off] = __float_as_uint(-INFINITY);
+      }
+      float smax = __uint_as_float(sv[0]);
+#pragma unroll
+      for (int c = 1; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
+      // the two key halves agree on the block maximum (rounded up to bf16)
+      const uint32_t mine = bf16_bits_up(smax);
+      st_async_b32(peer_xin + uint32_t((buf * kAttnBM + lrow) * 4), mine, peer_mx0 + 8u * buf);
+      if (!mbar_wait(&mx_full[buf], ph, flags)) {
+        alive = false;
+        break;
+      }
+      const uint32_t other = xin[buf * kAttnBM + lrow];
+      smax = fmaxf(bf16_bits_to_f32(mine), bf16_bits_to_f32(other));
+      const float bmax = smax * a.c_log2;
+      const float m_new = fmaxf(m_run, bmax);
+      const bool need = (m_run != -INFINITY) && (m_new > m_run + kRescaleLog2);
+      const float alpha = need ? exp2f(m_run - m_new) : 1.f;
+      if (need) {
+        l *= alpha;
+        m_run = m_new;
+      } else if (m_run == -INFINITY) {
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      uint32_t pk[32];
+      float l_lo = 0.f, l_hi = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = 2 * j;
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), a.c_log2, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), a.c_log2, -m_use));
+        if (a.vs_pre == nullptr) {
+          pk[j] = pack_bf16x2(p0, p1);
+          l_lo += __uint_as_float(pk[j] << 16);
+          l_hi += __uint_as_float(pk[j] & 0xffff0000u);
+        } else {
+          float sc[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int off = c + e;
+            sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + pos0 + off]
+                                  : a.vs_tail[(size_t)grp * a.Tpad + (pos0 - sq.P64) + off];
+          }
+          pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
+          const float w0 = __uint_as_float(pk[j] << 16), w1 = __uint_as_float(pk[j] & 0xffff0000u);
+          l_lo += sc[0] > 0.f ? w0 / sc[0] : 0.f;
+          l_hi += sc[1] > 0.f ? w1 / sc[1] : 0.f;
+        }
+      }
+      l += l_lo + l_hi;
+      tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      // P to the partner: its buffer is free once both pairs' P.V of block n - 2 finished
+      if (n >= 2 && !mbar_wait(&pv_done[buf], ((n - 2) >> 1) & 1, flags)) {
+        alive = false;
+        break;
+      }
+      {
+        const uint32_t row_addr = peer_sPO + uint32_t(buf * K::POBytes + lrow * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_async_v4(row_addr + uint32_t((j ^ (lrow & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                      pk[4 * j + 3], peer_po0 + 8u * buf);
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        if (!mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + uint32_t(cc * 32), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(tmem + lane_off + uint32_t(cc * 32), r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      // the partner's P has landed in this CTA's shared memory
+      if (!mbar_wait(&po_full[buf], ph, flags)) {
+        alive = false;
+        break;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(lead_p0 + 8u * buf);  // the pair leader issues P.V
+    }
+    if (alive && nb >= 1) {
+      alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
+      tc_fence_after();
+    }
+    // the two key halves' sums, through the exchange slot of block nb
+    float l_row = l;
+    if (alive) {
+      const int buf = nb & 1;
+      if (counter) mbar_arrive_expect_tx(&mx_full[buf], 4u * kAttnBM);
+      st_async_b32(peer_xin + uint32_t((buf * kAttnBM + lrow) * 4), __float_as_uint(l), peer_mx0 + 8u * buf);
+      alive = mbar_wait(&mx_full[buf], (nb >> 1) & 1, flags);
+      if (alive) l_row = l + __uint_as_float(xin[buf * kAttnBM + lrow]);
+    }
+    if (alive) {
+      const int hq = hk * a.G + g;
+      if (a.nsplit == 1) {
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)hq * a.d + pp * 256;
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + uint32_t(cc * 32), r);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              o[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+            uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
+        }
+        if (valid && pp == 0 && a.lse != nullptr)
+          a.lse[((size_t)b * a.C + i) * a.Hq + hq] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
+      } else if (qt < a.q_tiles) {
+        const size_t prow = ((size_t)split * a.B * a.Hkv + grp) * (size_t)(a.q_tiles * kAttnBM) + qt * kAttnBM + lrow;
+        float* dst = a.part_o + prow * a.d + pp * 256;
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t r[32];
+          if (nb >= 1) {
+            tmem_ld32(tmem + lane_off + uint32_t(cc * 32), r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          float4* o4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        if (pp == 0) {
+          a.part_ml[prow * 2] = m_run;
+          a.part_ml[prow * 2 + 1] = l_row;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // all four CTAs done with TMEM and with each other's shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 // One block of 128 threads per output row (b, KV head, packed row g*C + i):
 // merges the KV splits' partial rows by their running max and sum.
 __global__ void __launch_bounds__(128) attention_combine_kernel(AttnTcArgs a) {
@@ -1051,6 +1519,32 @@ cudaError_t launch_pair(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_
   return e;
 }
 
+cudaError_t launch_quad(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
+  static bool attr_set = false;
+  const int smem = Cfg4::Smem;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attention_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int clusters = a.B * a.Hkv * a.nsplit * ((a.q_tiles + 1) / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads4, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc4_kernel, maps, a);
+  count_launches(1);
+  return e;
+}
+
 }  // namespace
 
 size_t attention_tc_smem_bytes(int d) {
@@ -1068,7 +1562,8 @@ cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cud
     case 64: return launch_d<64>(maps, a, stream);
     case 128: return launch_d<128>(maps, a, stream);
     case 256: return a.pair ? launch_pair<256>(maps, a, stream) : launch_d<256>(maps, a, stream);
-    case 512: return a.pair ? launch_pair<512>(maps, a, stream) : launch_d<512>(maps, a, stream);
+    case 512: return a.pair == 2 ? launch_quad(maps, a, stream)
+                                 : a.pair ? launch_pair<512>(maps, a, stream) : launch_d<512>(maps, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

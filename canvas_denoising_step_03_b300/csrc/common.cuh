@@ -58,11 +58,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa),
-// release semantics at cluster scope: this thread's earlier shared::cluster
-// stores are visible to threads that observe the phase flip.
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa).
+// Default (CTA-scope) semantics: the only data that crosses CTAs through these
+// barriers is tensor memory, ordered by the tcgen05 fences around the arrive
+// and the wait; a cluster-scope release here would cost a memory barrier per
+// arrive.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
@@ -77,30 +79,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
-// Acquire at cluster scope: pairs with mbar_arrive_remote from another CTA.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for the phase of parity `parity` of `bar` to complete.  Gives up when
 // *abort is set by another thread of the CTA, or after the timeout, in which
 // case it sets *abort, records CANVAS_ERR_TIMEOUT and returns false.  The
 // first probe is inline; the polling loop is a separate function, so its
 // register saves stay off the path where the phase is already complete.
-template <bool kCluster = false>
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > CANVAS_WAIT_TIMEOUT_NS) {
@@ -112,11 +100,9 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, vola
   }
 }
 
-template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const uint32_t a = smem_u32(bar);
-  if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-  return mbar_wait_slow<kCluster>(bar, parity, abort);
+  if (mbar_try_wait(smem_u32(bar), parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,6 +133,24 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 // generic-proxy writes to shared memory -> visible to the async proxy (TMA,
 // tensor core operand reads)
+// TMA tiled store of a shared-memory box to global memory (bulk-group
+// completion: commit_group, then wait_group before the box is rewritten and
+// before the CTA exits).  Coordinates are never negative here.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all but the newest N committed groups have finished reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// every committed group has completed (its writes performed)
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -339,6 +343,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+// Asynchronous stores into another CTA's shared memory (addresses from mapa)
+// that complete on that CTA's mbarrier (complete_tx of the stored bytes).
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(remote_bar)
+               : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -373,23 +391,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // cos / sin of the RoPE angle pos * freq.  freq is split into turns,
-// g = freq / (2 pi) = g_hi + g_lo (two fp32 parts of the fp64 quotient).
-// pos * g_hi = t + e exactly (FMA two-product, Ogita-Rump-Oishi), t - rint(t)
-// is exact, so the fraction of a turn f carries an absolute error near 2^-25
-// for every pos < 2^24; sincospif then evaluates sin / cos of 2*pi*f.
+// g = freq / (2 pi) = g_hi + g_lo: the product of freq with 1 / (2 pi) held
+// as two fp32 parts (c_hi + c_lo, residual below 2^-50 relative), the rounding
+// error of freq * c_hi recovered exactly by an FMA (two-product,
+// Ogita-Rump-Oishi), so g_hi + g_lo carries about 46 correct bits without any
+// fp64 arithmetic.  pos * g_hi = t + e exactly (two-product again),
+// t - rint(t) is exact, so the fraction of a turn f carries an absolute error
+// near 2^-25 for every pos < 2^24; sincospif then evaluates sin / cos of
+// 2*pi*f.
 struct RopeTurns {
   float hi, lo;
 };
 __device__ __forceinline__ RopeTurns rope_turns(float freq) {
-  const double g = double(freq) * 0.15915494309189533576888376337251;  // 1 / (2 pi)
+  const float c_hi = __int_as_float(0x3E22F983);  // fp32(1 / (2 pi))
+  const float c_lo = __int_as_float(0x31DC9C88);  // fp32(1 / (2 pi) - c_hi)
   RopeTurns r;
-  r.hi = float(g);
-  r.lo = float(g - double(r.hi));
+  r.hi = __fmul_rn(freq, c_hi);
+  r.lo = fmaf(freq, c_lo, fmaf(freq, c_hi, -r.hi));
   return r;
 }
 __device__ __forceinline__ void rope_cos_sin(int pos, RopeTurns g, float* c, float* s) {
   const float p = float(pos);
-  const float t = p * g.hi;
+  const float t = __fmul_rn(p, g.hi);  // kept apart from the FMAs below
   const float e = fmaf(p, g.hi, -t);
   const float f = (t - rintf(t)) + (e + p * g.lo);
   sincospif(2.0f * f, s, c);

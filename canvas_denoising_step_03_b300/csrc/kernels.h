@@ -35,20 +35,31 @@ struct SampleArgs {
 cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, cudaStream_t stream);
 
 // ----------------------------------------------------------------- GEMMs
-// tcgen05 bf16 GEMM: C[M,N] (fp32) = A[M,K] * op(B)
+// tcgen05 bf16 GEMM, up to three problems sharing A and K (the q / k / v
+// projections of one x): C_p[M,N_p] = A[M,K] * op(B_p), fp32 (or bf16) out.
+constexpr int kGemmMaxProblems = 3;
 struct GemmTcArgs {
-  float* C;
-  int M, N, K, ldc;
-  int accumulate;
+  int M, K, kblocks, splits;
+  int accumulate;  // C += (one problem)
+  int out_bf16;    // C holds bf16 (no accumulate)
   int b_mn_major;  // 0: B is [N,K] (K contiguous); 1: B is [K,N] (N contiguous)
   int two_acc;     // 1: a CTA covers 256 rows (two 128-row accumulators)
-  int m_tiles, n_tiles, splits, kblocks;
-  float* partials;  // [splits][M][N] when splits > 1 (ldc == N), summed by a reduce kernel
+  int m_tiles, nprob;
+  int tile0[kGemmMaxProblems + 1];  // first 256-column tile of each problem; tile0[nprob] = all tiles
+  int N[kGemmMaxProblems];
+  void* C[kGemmMaxProblems];
+  float* partials[kGemmMaxProblems];  // [splits][M][N_p] when splits > 1, summed by a reduce kernel
+};
+// A (K-major bf16), B of each problem, and the TMA store target of each
+// problem (C, or the split partials)
+struct GemmTcMaps {
+  CUtensorMap A;
+  CUtensorMap B[kGemmMaxProblems];
+  CUtensorMap out[kGemmMaxProblems];
 };
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 3;
 size_t gemm_tc_smem_bytes();
-cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmTcArgs& g,
-                           cudaStream_t stream);
+cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStream_t stream);
 
 // SIMT GEMM (fp32 path): C[M,N] = A[M,K] * op(B) (+C), TA/TB = float or bf16
 cudaError_t launch_gemm_simt(const void* A, const void* B, int b_mn_major, bool bf16, float* C, int M, int N,
@@ -139,7 +150,9 @@ constexpr int kAttnBN = 128;       // keys per block
 struct AttnTcArgs {
   int B, C, Hq, Hkv, G, d, DV, dv_parts, q_tiles, nsplit, max_prefix, window, Tpad;
   int kpre_paged;            // 1: prefix keys from the paged pool; 0: dense Kt
-  int pair;                  // 1: 2-SM kernel (CTA pairs share each MMA), head_dim 256 / 512
+  int pair;                  // 1: 2-SM kernel (CTA pairs share each MMA), head_dim 256 / 512;
+                             // 2: 4-SM kernel (two pairs split the key blocks), head_dim 512
+  const __nv_bfloat16* Qp;   // [B][Hkv][G][C][d] prepared queries (the 4-SM kernel reads half of each row)
   const int32_t* block_table;
   int max_pages, page_tokens, num_pages;
   const int32_t* prefix_len;
@@ -153,6 +166,7 @@ struct AttnTcArgs {
 };
 struct AttnTcMaps {
   CUtensorMap q, kpre, vpre, kx, vx;
+  CUtensorMap kpre32, kx32;  // keys in 32-row boxes (the 4-SM kernel)
 };
 size_t attention_tc_smem_bytes(int d);
 cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream);

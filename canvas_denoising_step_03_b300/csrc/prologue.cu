@@ -21,6 +21,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace canvas {
 
 namespace {
@@ -239,22 +241,12 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
   }
 }
 
-// One warp per (b, KV head, row).  Rows [0, max_prefix) (global layers only):
-// prefix keys Kt and value scalars for positions below P64.  Rows
-// [max_prefix, max_prefix + Tpad): tail row t = row - max_prefix -- prefix
-// rows P64 + t < P are gathered from the cache, rows past the canvas are
-// zeroed, canvas rows are left to the prologue kernel.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__device__ __forceinline__ void key_prep_row(const KeyPrepArgs& k, int w, int row0, int L) {
   const int lane = threadIdx.x & 31;
-  const int row0 = k.global ? 0 : k.max_prefix;
-  const int L = k.max_prefix + k.Tpad - row0;
-  const int total = k.B * k.Hkv * L;
-  if (warp_global >= total) return;
-  const int row = row0 + warp_global % L;
-  const int hk = (warp_global / L) % k.Hkv;
-  const int b = warp_global / (L * k.Hkv);
+  const int row = row0 + w % L;
+  const int hk = (w / L) % k.Hkv;
+  const int b = w / (L * k.Hkv);
   const int P = k.prefix_len[b];
   if (P < 0 || P > k.max_prefix) {
     if (lane == 0 && row == row0 && hk == 0) record_error(CANVAS_ERR_BOUNDS);
@@ -306,6 +298,22 @@ __global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
   }
 }
 
+// One warp per (b, KV head, row), grid-stride over the rows.  Rows
+// [0, max_prefix) (global layers only): prepared prefix keys Kt and value
+// scalars for positions below P64.  Rows [max_prefix, max_prefix + Tpad):
+// tail row t = row - max_prefix -- prefix rows P64 + t < P are gathered from
+// the cache, rows past the canvas are zeroed, canvas rows are left to the
+// prologue kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
+  const int row0 = k.global ? 0 : k.max_prefix;
+  const int L = k.max_prefix + k.Tpad - row0;
+  const int total = k.B * k.Hkv * L;
+  const int nwarps = int((gridDim.x * blockDim.x) >> 5);
+  for (int w = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5); w < total; w += nwarps)
+    key_prep_row<T, D>(k, w, row0, L);
+}
+
 template <typename T>
 cudaError_t launch_prologue_t(const PrologueArgs& p, int blocks, cudaStream_t stream) {
   if (sizeof(T) == 2 && (p.d & (p.d - 1)) != 0) return cudaErrorInvalidValue;
@@ -323,21 +331,34 @@ cudaError_t launch_prologue_t(const PrologueArgs& p, int blocks, cudaStream_t st
   return cudaGetLastError();
 }
 
+// grid-stride launch: as many 256-thread blocks as fit on the 148 SMs at once
+template <typename T, int D>
+cudaError_t launch_key_prep_d(const KeyPrepArgs& k, long long blocks_needed, cudaStream_t stream) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, key_prep_kernel<T, D>, 256, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = std::max(per_sm, 1);
+  }
+  const int blocks = int(std::max(1LL, std::min<long long>(blocks_needed, 148LL * per_sm)));
+  key_prep_kernel<T, D><<<blocks, 256, 0, stream>>>(k);
+  return cudaGetLastError();
+}
+
 template <typename T>
-cudaError_t launch_key_prep_t(const KeyPrepArgs& k, int blocks, cudaStream_t stream) {
+cudaError_t launch_key_prep_t(const KeyPrepArgs& k, long long blocks, cudaStream_t stream) {
   if (sizeof(T) == 2 && (k.d & (k.d - 1)) != 0) return cudaErrorInvalidValue;
   switch (k.d) {
-    case 64: key_prep_kernel<T, 64><<<blocks, 256, 0, stream>>>(k); break;
-    case 128: key_prep_kernel<T, 128><<<blocks, 256, 0, stream>>>(k); break;
-    case 256: key_prep_kernel<T, 256><<<blocks, 256, 0, stream>>>(k); break;
-    case 512: key_prep_kernel<T, 512><<<blocks, 256, 0, stream>>>(k); break;
-    case 192: key_prep_kernel<T, 192><<<blocks, 256, 0, stream>>>(k); break;
-    case 320: key_prep_kernel<T, 320><<<blocks, 256, 0, stream>>>(k); break;
-    case 384: key_prep_kernel<T, 384><<<blocks, 256, 0, stream>>>(k); break;
-    case 448: key_prep_kernel<T, 448><<<blocks, 256, 0, stream>>>(k); break;
+    case 64: return launch_key_prep_d<T, 64>(k, blocks, stream);
+    case 128: return launch_key_prep_d<T, 128>(k, blocks, stream);
+    case 256: return launch_key_prep_d<T, 256>(k, blocks, stream);
+    case 512: return launch_key_prep_d<T, 512>(k, blocks, stream);
+    case 192: return launch_key_prep_d<T, 192>(k, blocks, stream);
+    case 320: return launch_key_prep_d<T, 320>(k, blocks, stream);
+    case 384: return launch_key_prep_d<T, 384>(k, blocks, stream);
+    case 448: return launch_key_prep_d<T, 448>(k, blocks, stream);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -353,7 +374,7 @@ cudaError_t launch_prologue(const PrologueArgs& p, bool bf16, cudaStream_t strea
 cudaError_t launch_key_prep(const KeyPrepArgs& k, bool bf16, cudaStream_t stream) {
   const int rows = (k.global ? k.max_prefix : 0) + k.Tpad;
   const long long warps = (long long)k.B * k.Hkv * rows;
-  const int blocks = int((warps * 32 + 255) / 256);
+  const long long blocks = (warps * 32 + 255) / 256;
   count_launches(1);
   return bf16 ? launch_key_prep_t<__nv_bfloat16>(k, blocks, stream) : launch_key_prep_t<float>(k, blocks, stream);
 }

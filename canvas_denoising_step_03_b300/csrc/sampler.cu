@@ -206,11 +206,18 @@ __device__ __forceinline__ RowState reduce_row(RowState s, RowState* warp_part, 
   return t;
 }
 
-// bf16 logits, the slice staged in shared memory by one bulk copy (up to
-// 64 KB): the HBM read is issued at once and overlaps the cluster start-up,
-// both passes read shared memory, and three CTAs fit on an SM so one CTA's
-// loads overlap another's arithmetic.
+// bf16 logits, the slice staged in shared memory (up to 64 KB) by bulk copies
+// of 16 KB, each completing on its own mbarrier: the whole HBM read is issued
+// at once, the first pass starts on the first piece while the others are in
+// flight, both passes read shared memory, and three CTAs fit on an SM.  The
+// partial states are exchanged with st.async (distributed shared memory
+// stores that complete on the receiving CTA's mbarrier), so the reduction
+// needs no cluster-wide barrier; one cluster barrier, split into an arrive
+// after the exchange and a wait before exit, keeps every CTA alive until all
+// stores into it have landed.
 constexpr int kSmemSliceBytes = 65536;
+constexpr int kPieceElems = 8192;
+constexpr int kMaxPieces = kSmemSliceBytes / (2 * kPieceElems);
 
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a,
@@ -218,8 +225,9 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   constexpr int kWarps = kThreads / 32;
   extern __shared__ __align__(128) uint8_t slice_raw[];
   __shared__ RowState warp_part[kWarps];
-  __shared__ float cl_part[kMaxSampleCluster][5];
-  __shared__ uint64_t full;
+  __shared__ __align__(16) uint32_t cl_msg[kMaxSampleCluster][8];
+  __shared__ uint64_t full[kMaxPieces];
+  __shared__ uint64_t red_bar;
   __shared__ int abort_flag;
   const int row = blockIdx.y;
   const uint32_t rank = cluster_ctarank();
@@ -230,36 +238,95 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   const __nv_bfloat16* src = logits + (long long)row * a.V + c0;
   const __nv_bfloat16* slice = reinterpret_cast<const __nv_bfloat16*>(slice_raw);
   if (threadIdx.x == 0) {
-    mbar_init(&full, 1);
+    for (int p = 0; p < kMaxPieces; ++p) mbar_init(&full[p], 1);
+    mbar_init(&red_bar, 1);
     abort_flag = 0;
     fence_mbarrier_init();
-    mbar_arrive_expect_tx(&full, uint32_t(n) * 2u);
-    for (int off = 0; off < n; off += 8192)  // 16 KB pieces
-      bulk_load(slice_raw + off * 2, src + off, uint32_t(min(8192, n - off)) * 2u, &full);
+    // this thread's arrival plus the bytes of every CTA's partial state
+    mbar_arrive_expect_tx(&red_bar, csize * 32u);
+    for (int p = 0; p * kPieceElems < n; ++p) {
+      const uint32_t cnt = uint32_t(min(kPieceElems, n - p * kPieceElems));
+      mbar_arrive_expect_tx(&full[p], cnt * 2u);
+      bulk_load(slice_raw + p * kPieceElems * 2, src + p * kPieceElems, cnt * 2u, &full[p]);
+    }
   }
-  // every CTA of the cluster is running before any DSMEM store (in reduce_row)
-  cluster_sync_all();
-  // on a timeout the status word is set and the CTA carries on, so that no
-  // peer waits for it at a cluster barrier
-  mbar_wait(&full, 0, &abort_flag);
+  // every CTA's barriers are initialised before any peer stores into it (the
+  // initialising thread's fence.mbarrier_init releases them; the arrive
+  // itself needs no memory ordering)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   const float ysc = a.inv_temp * kLog2e;
   RowState s;
   state_init(s);
-  for (int i = threadIdx.x * 8; i < n; i += kThreads * 8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    float x[8];
+  for (int p = 0; p * kPieceElems < n; ++p) {
+    // on a timeout the status word is set and the CTA carries on, so that
+    // no peer waits for it
+    mbar_wait(&full[p], 0, &abort_flag);
+    const int e = min(n, (p + 1) * kPieceElems);
+    for (int i = p * kPieceElems + threadIdx.x * 8; i < e; i += kThreads * 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      float x[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = __uint_as_float(w[j] << 16);
-      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      }
+      state_add8(s, x, ysc, int(c0) + i);
     }
-    state_add8(s, x, ysc, int(c0) + i);
   }
-  const RowState t = reduce_row<kThreads>(s, warp_part, cl_part, rank, csize);
-  if (threadIdx.x == 0 && rank == 0) row_decision(a, row, t);
+  // warp, then CTA, then cluster (every CTA merges the partial states in
+  // rank order, so all end with the same bits)
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    RowState o;
+    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+    o.Z = __shfl_xor_sync(0xffffffffu, s.Z, off);
+    o.T = __shfl_xor_sync(0xffffffffu, s.T, off);
+    o.bx = __shfl_xor_sync(0xffffffffu, s.bx, off);
+    o.bi = __shfl_xor_sync(0xffffffffu, s.bi, off);
+    RowState lo = (threadIdx.x & off) ? o : s;
+    const RowState hi = (threadIdx.x & off) ? s : o;
+    state_merge(lo, hi);
+    s = lo;
+  }
+  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RowState t = warp_part[0];
+    for (int w = 1; w < kWarps; ++w) state_merge(t, warp_part[w]);
+    const uint32_t msg = smem_u32(&cl_msg[rank][0]), bar = smem_u32(&red_bar);
+    for (uint32_t dst = 0; dst < csize; ++dst) {
+      const uint32_t ra = mapa_shared(msg, dst), rb = mapa_shared(bar, dst);
+      st_async_v4(ra, __float_as_uint(t.m), __float_as_uint(t.Z), __float_as_uint(t.T), __float_as_uint(t.bx), rb);
+      st_async_v4(ra + 16, uint32_t(t.bi), 0u, 0u, 0u, rb);
+    }
+  }
+  // one warp merges the partial states in rank order and publishes the row's
+  // maximum and 1 / Z to the CTA
+  if (threadIdx.x < 32) {
+    mbar_wait(&red_bar, 0, &abort_flag);
+    RowState t;
+    state_init(t);
+    for (uint32_t r = 0; r < csize; ++r) {
+      RowState o;
+      o.m = __uint_as_float(cl_msg[r][0]);
+      o.Z = __uint_as_float(cl_msg[r][1]);
+      o.T = __uint_as_float(cl_msg[r][2]);
+      o.bx = __uint_as_float(cl_msg[r][3]);
+      o.bi = int(cl_msg[r][4]);
+      state_merge(t, o);
+    }
+    if (threadIdx.x == 0) {
+      warp_part[0].m = t.m;
+      warp_part[0].Z = 1.0f / t.Z;
+      if (rank == 0) row_decision(a, row, t);
+    }
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const RowState t = warp_part[0];  // m and 1 / Z
   const float M = t.m;
-  const float invZ = 1.0f / t.Z;
+  const float invZ = t.Z;
   for (int i = threadIdx.x * 8; i < n; i += kThreads * 8) {
     const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -284,6 +351,7 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
       q[1] = make_float4(p[4], p[5], p[6], p[7]);
     }
   }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 template <typename T, int kThreads>

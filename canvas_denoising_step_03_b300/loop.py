@@ -9,7 +9,8 @@ One step, for B canvases of C tokens:
 2. per layer: ``canvas_attention`` on the bf16 stream, then
    ``canvas_gemm_bf16`` adds out W_o^T to the fp32 stream and
    ``canvas_cast_bf16`` refreshes the bf16 copy;
-3. tied LM head: ``canvas_gemm_bf16`` computes x E^T (fp32), cast to bf16;
+3. tied LM head: ``canvas_gemm_bf16_to_bf16`` computes x E^T, accumulated in
+   fp32 and stored once as bf16 logits;
 4. ``canvas_sample`` with the step index; positions committed in earlier
    steps stay frozen with their tokens.
 
@@ -24,7 +25,8 @@ import torch
 
 from . import (CANVAS_BF16, CANVAS_LAYER_GLOBAL, CANVAS_LAYER_SLIDING, canvas_attention,
                canvas_attention_workspace_size, canvas_cast_bf16, canvas_embed_input, canvas_gemm_bf16,
-               canvas_gemm_workspace_size, canvas_sample, canvas_sample_workspace_size, make_kv_cache, workspace)
+               canvas_gemm_bf16_to_bf16, canvas_gemm_workspace_size, canvas_sample, canvas_sample_workspace_size,
+               make_kv_cache, workspace)
 
 
 def _bf16(a: np.ndarray, device) -> torch.Tensor:
@@ -66,7 +68,6 @@ class CanvasLoop:
         self.tokens = torch.from_numpy(inp.tokens0.astype(np.int32)).to(device)
         self.x = torch.empty((B, C, D), dtype=torch.bfloat16, device=device)
         self.x32 = torch.empty((R, D), dtype=torch.float32, device=device)
-        self.logits32 = torch.empty((R, V), dtype=torch.float32, device=device)
         self.logits = torch.empty((R, V), dtype=torch.bfloat16, device=device)
         self.soft = torch.zeros((R, D), dtype=torch.float32, device=device)
         self.frozen = torch.zeros(R, dtype=torch.uint8, device=device)
@@ -105,8 +106,7 @@ class CanvasLoop:
     def head(self, x: torch.Tensor) -> torch.Tensor:
         """bf16 logits of the tied LM head, x E^T."""
         R = self.cfg.B * self.cfg.C
-        canvas_gemm_bf16(x.view(R, -1), self.E, 0, self.logits32, 0, self.gemm_ws)
-        canvas_cast_bf16(self.logits32, self.logits)
+        canvas_gemm_bf16_to_bf16(x.view(R, -1), self.E, 0, self.logits, self.gemm_ws)
         return self.logits
 
     def sample(self, logits: torch.Tensor, step: int, frozen: torch.Tensor, frozen_tokens: torch.Tensor):
@@ -117,17 +117,26 @@ class CanvasLoop:
                       self.next_tokens, self.mask, self.entropy, self.conf, self.argmax, None, CANVAS_BF16,
                       self.soft, self.samp_ws)
 
-    def step(self, keep_attn: bool = False):
+    def step(self, keep_attn: bool = False, mark=None):
         """Run one denoising step on the loop's own state; returns the
-        attention outputs if asked."""
+        attention outputs if asked.  ``mark(name)``, if given, is called on the
+        host between the stages (``attention_begin``/``attention_end`` around
+        each layer's attention call, ``sample_begin``/``sample_end`` around the
+        sampler call), e.g. to record CUDA events on the stream."""
+        mark = mark or (lambda name: None)
         self.embed(self.tokens, self.soft if self.step_index > 0 else None)
         outs = []
         for k in range(len(self.layers)):
+            mark("attention_begin")
             out = self.attention(k, self.x)
+            mark("attention_end")
             if keep_attn:
                 outs.append(out.clone())
             self.residual(k, out, self.x32, self.x)
-        self.sample(self.head(self.x), self.step_index, self.frozen, self.tokens)
+        logits = self.head(self.x)
+        mark("sample_begin")
+        self.sample(logits, self.step_index, self.frozen, self.tokens)
+        mark("sample_end")
         # committed positions stay frozen with their tokens in the next step
         self.tokens, self.next_tokens = self.next_tokens, self.tokens
         self.frozen.copy_(self.mask)

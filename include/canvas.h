@@ -209,11 +209,28 @@ size_t canvas_gemm_workspace_size(int M, int N, int K);
  *   B  b_layout 0: [N, K] row-major ("weights", C = A B^T)
  *      b_layout 1: [K, N] row-major (C = A B)
  *   C  [M, N] fp32 row-major, leading dimension N
- * Requires K % 8 == 0 and N % 8 == 0 (16-byte aligned rows).
+ * Requires K % 8 == 0 and N % 8 == 0 (16-byte aligned rows) and A, B, C
+ * 16-byte aligned (CANVAS_ERR_ARG otherwise).
  */
 canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float* C,
                                int M, int N, int K, int accumulate,
                                void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
+/*
+ * canvas_gemm_bf16_to_bf16 -- C[M,N] (bf16) = bf16(A[M,K] . op(B)).
+ *
+ * The same product as canvas_gemm_bf16, accumulated in fp32 and rounded once
+ * to bf16 (nearest even) where it is stored: the tied LM head of a denoising
+ * step writes its logits this way, the form canvas_sample reads ([AIT]
+ * "섹션별 상세", sampling-loop paragraph), without an fp32 copy of them.
+ *   A, B, b_layout, M, N, K, workspace  as for canvas_gemm_bf16 (same
+ *                                       workspace size)
+ *   C  [M, N] bf16 row-major, leading dimension N, 16-byte aligned
+ * Errors as for canvas_gemm_bf16.  Asynchronous on `stream`.
+ */
+canvas_status canvas_gemm_bf16_to_bf16(const void* A, const void* B, int b_layout, void* C,
+                                       int M, int N, int K,
+                                       void* workspace, size_t ws_bytes, canvas_stream_t stream);
 
 /*
  * canvas_embed_input -- the canvas input of a denoising step:

@@ -104,6 +104,9 @@ def test_tiny_fp32_workload(cv):
     small(layer="global", window=0, theta=1e6, rotary_fraction=0.25),
     small(layer="global", window=0, theta=1e6, rotary_fraction=0.25, Hq=8, Hkv=1, d=512, D=512,
           prefix=(200, 64), C=64),
+    small(layer="global", window=0, theta=1e6, rotary_fraction=0.25, Hq=8, Hkv=1, d=512, D=512,
+          prefix=(0, 130), C=48),                              # head_dim 512: odd number of 128-row tiles, empty prefix
+    small(layer="sliding", window=100, Hq=4, Hkv=2, d=512, D=512, prefix=(330, 70), C=40),  # head_dim 512 with a window
     small(dtype="fp32", page_tokens=16),
     small(dtype="fp32", layer="global", window=0, theta=1e6, rotary_fraction=0.25, page_tokens=32),
 ], ids=lambda c: f"{c.layer}-{c.dtype}-B{c.B}C{c.C}P{'_'.join(map(str, c.prefix))}-H{c.Hq}x{c.Hkv}d{c.d}w{c.window}")
@@ -113,6 +116,11 @@ def test_small_shapes(cv, cfg):
 
 def test_global_unit_rms_value_variant(cv):
     check(cv, small(layer="global", window=0, theta=1e6, rotary_fraction=0.25), v_unit_rms=True)
+
+
+def test_global_unit_rms_value_variant_head_dim_512(cv):
+    check(cv, small(layer="global", window=0, theta=1e6, rotary_fraction=0.25, Hq=8, Hkv=1, d=512, D=512,
+                    prefix=(500,), B=1, C=64), v_unit_rms=True)
 
 
 def test_page_permutation_does_not_change_the_result(cv):

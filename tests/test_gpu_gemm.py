@@ -53,8 +53,15 @@ def test_gemm_matches_fp64(cv, M, N, K, b_layout):
 
 
 def test_gemm_accumulate(cv):
-    err, mx = _run(cv, 256, 512, 2048, 0, accumulate=1)
+    err, mx = _run(cv, 256, 512, 2048, 0, accumulate=1)   # K split: the reduce kernel adds C
     assert err < 5e-5, err
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 64), (100, 200, 120)])
+def test_gemm_accumulate_single_split(cv, M, N, K):
+    # one K split: the GEMM's own epilogue adds into C (ragged edges included)
+    err, mx = _run(cv, M, N, K, 0, accumulate=1)
+    assert err < 5e-5 and mx < 5e-4, (err, mx)
 
 
 def test_gemm_repeatable_bitwise(cv):
@@ -70,3 +77,24 @@ def test_gemm_repeatable_bitwise(cv):
         outs.append(C)
     assert cv.canvas_device_status() == cv.CANVAS_OK
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("M,N,K,b_layout", [
+    (1024, 4096, 2816, 0),  # K split: the reduce kernel rounds
+    (256, 520, 64, 0),      # one split, ragged N: the epilogue's 64-column bf16 boxes are clipped
+    (100, 200, 136, 1),     # ragged M, N, K, B stored [K, N]
+])
+def test_gemm_bf16_output_is_the_rounded_fp32_product(cv, M, N, K, b_layout):
+    """canvas_gemm_bf16_to_bf16 equals canvas_gemm_bf16 rounded to bf16
+    (nearest even), bit for bit: the same accumulation, one rounding."""
+    g = torch.Generator(device="cuda").manual_seed(M + N)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = (torch.randn(N, K, device="cuda", generator=g) if b_layout == 0 else
+         torch.randn(K, N, device="cuda", generator=g)).to(torch.bfloat16)
+    ws = cv.workspace(cv.canvas_gemm_workspace_size(M, N, K))
+    C32 = torch.empty(M, N, device="cuda")
+    cv.canvas_gemm_bf16(A, B, b_layout, C32, 0, ws)
+    C16 = torch.full((M, N), float("nan"), device="cuda", dtype=torch.bfloat16)
+    cv.canvas_gemm_bf16_to_bf16(A, B, b_layout, C16, ws)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    assert torch.equal(C16.view(torch.int16), C32.to(torch.bfloat16).view(torch.int16))
