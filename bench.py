@@ -185,6 +185,19 @@ class ClockSampler:
                 "power_w_max": round(max(pw), 1) if pw else None, "source": "nvml"}
 
 
+def max_over_ranks(values, device=None):
+    """Elementwise maximum of a list of floats over every rank of the process
+    group (the step time of a multi-GPU run is its slowest rank's); a plain
+    copy when there is one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 # --------------------------------------------------------------------------- our arm
 class Step:
     """Device state of one canvas step (attention + sampler)."""
@@ -298,11 +311,7 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     kern_ms = {names[kid]: statistics.mean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
                for j, kid in enumerate(ids)}
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([statistics.mean(step_ms)], dev)[0]
 
     # ---- end to end: host inputs (pinned) -> device, results -> host, every step
     x_h = torch.empty(st.x.shape, dtype=torch.bfloat16).pin_memory()
@@ -335,11 +344,7 @@ def run_ours(args, rank, world, local_rank):
             oh.copy_(o, non_blocking=True)
         e2e_ev[k][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks([statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)], dev)[0]
     assert cv.canvas_device_status() == cv.CANVAS_OK
 
     if rank != 0:
@@ -451,12 +456,8 @@ def run_loop(args, rank, world, local_rank):
         attn_ms.append(sum(per))
         sm = {n: e for n, e in marks if n.startswith("sample")}
         samp_ms.append(sm["sample_begin"].elapsed_time(sm["sample_end"]))
-    ms_core = statistics.mean(a + s_ for a, s_ in zip(attn_ms, samp_ms))
-    ms_step = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_core, ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_core, ms_step = (float(v) for v in t.tolist())
+    ms_core, ms_step = max_over_ranks([statistics.mean(a + s_ for a, s_ in zip(attn_ms, samp_ms)),
+                                       statistics.mean(step_ms)], dev)
     # end to end: the step's result (tokens, commit mask) read back to pinned
     # host memory inside every timed step
     tok_h = torch.empty(run.tokens.shape, dtype=run.tokens.dtype).pin_memory()
@@ -469,11 +470,7 @@ def run_loop(args, rank, world, local_rank):
         mask_h.copy_(run.mask, non_blocking=True)
         e2e.append((t0, new_ev()))
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks([statistics.mean(a.elapsed_time(b) for a, b in e2e)], dev)[0]
     if rank != 0:
         return None
     lcs = cfg.layer_cfgs()

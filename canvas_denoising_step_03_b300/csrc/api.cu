@@ -484,6 +484,8 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   const bool bf16 = dtype == CANVAS_BF16;
   if (!x || !W_q || !W_k || !gamma_q || !gamma_k || !freq || !kv || !prefix_len || !out)
     return fail(CANVAS_ERR_ARG, "canvas_attention: null pointer");
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_attention: x and out must be 16-byte aligned");
   if (global && W_v != nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: global layers share W_v = W_k (pass NULL)");
   if (!global && W_v == nullptr) return fail(CANVAS_ERR_ARG, "canvas_attention: sliding layers need W_v");
   if (v_unit_rms && !global) return fail(CANVAS_ERR_ARG, "canvas_attention: v_unit_rms applies to global layers");
@@ -606,7 +608,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
       maps.vpre = maps.vx;
     }
     // the 4-SM kernel (head_dim 512) reads keys in 32-row boxes
-    const bool quad = false;  // d == 512 once validated
+    const bool quad = d == 512;
     if (quad) {
       st = make_map_bf16(&maps.kx32, Kx, BH * pl.Tpad, d, 32, 64);
       if (st != CANVAS_OK) return st;

@@ -985,20 +985,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // into shared memory, so both pairs form O over all 128 keys:
 //   O_p += P_own V[own keys, half p]   (P from TMEM, where the softmax wrote it)
 //        + P_other V[other keys, half p]  (P from shared memory).
-// Half of Q (d 0..255) sits in TMEM, the other half in shared memory, which
-// leaves room for a four-stage ring (two blocks of K and V in flight).
-// TMEM columns: O [0, 256), S / P [256, 320) and [320, 384), Q [384, 512).
+// NS S buffers: with three, the softmax of a block (with its two exchanges
+// between CTAs) overlaps the MMAs of the next two blocks, a quarter of Q
+// (d 0..127) sits in TMEM and the ring has three stages; with two, half of Q
+// sits in TMEM and the ring has four stages (two blocks of K and V in flight).
+// TMEM columns: O [0, 256), S / P NS x 64 from 256, Q at 256 + 64 NS.
+template <int NS>
 struct Cfg4 {
-  static constexpr int NST = 4;
-  static constexpr int QSBytes = 4 * 16384;  // Q d 256..511: four 64-wide chunks of 128 rows
+  static constexpr int NST = NS == 2 ? 4 : 3;
+  static constexpr int QT = NS == 2 ? 4 : 2;        // 64-wide chunks of Q held in TMEM
+  static constexpr int QSBytes = (8 - QT) * 16384;  // the other chunks in shared memory (128 rows each)
   static constexpr int POBytes = 16384;      // the partner's P: 128 rows x 64 keys bf16
   static constexpr int Smem = QSBytes + 2 * POBytes + NST * kStageBytes + 1024 + kBarBytes + 1024;
 };
 constexpr int kThreads4 = 192;  // TMA warp, MMA warp, 4 softmax / epilogue warps
 
+template <int NS>
 __global__ void __launch_bounds__(kThreads4, 1)
     attention_tc4_kernel(const __grid_constant__ AttnTcMaps maps, AttnTcArgs a) {
-  using K = Cfg4;
+  using K = Cfg4<NS>;
   constexpr int D = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1009,15 +1014,16 @@ __global__ void __launch_bounds__(kThreads4, 1)
   uint64_t* empty = full + K::NST;
   uint64_t* q_full = empty + K::NST;
   uint64_t* qt_ready = q_full + 1;
-  uint64_t* s_full = qt_ready + 1;  // [2]
-  uint64_t* p_full = s_full + 2;    // [2] (pair leader)
-  uint64_t* pv_done = p_full + 2;   // [2] both pairs' P.V of a block
+  uint64_t* s_full = qt_ready + 1;  // [NS]
+  uint64_t* p_full = s_full + NS;   // [NS] (pair leader) this pair's P in TMEM
+  uint64_t* px_full = p_full + NS;  // [NS] (pair leader) the other pair's P in shared memory
+  uint64_t* pv_done = px_full + NS; // [2] both pairs' P.V of a block
   uint64_t* mx_full = pv_done + 2;  // [2] the partner's maxima (and, last, its sums)
   uint64_t* po_full = mx_full + 2;  // [2] the partner's P
   uint64_t* drain = po_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
-  static_assert((2 * K::NST + 2 + 2 * 5 + 1) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * K::NST + 2 + 3 * NS + 2 * 3 + 1) * 8 + 8 <= kBarBytes, "barrier area");
   uint32_t* xin = reinterpret_cast<uint32_t*>(ring + K::NST * kStageBytes + kBarBytes);  // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1050,9 +1056,12 @@ __global__ void __launch_bounds__(kThreads4, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(qt_ready, 8);  // the softmax warps of both CTAs of the pair
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < NS; ++j) {
       mbar_init(&s_full[j], 1);
       mbar_init(&p_full[j], 8);
+      mbar_init(&px_full[j], 8);
+    }
+    for (int j = 0; j < 2; ++j) {
       mbar_init(&pv_done[j], 2);  // one commit from each pair's leader
       mbar_init(&mx_full[j], 1);
       mbar_init(&po_full[j], 1);
@@ -1074,7 +1083,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
   cluster_sync_all();  // barriers of all four CTAs initialised, TMEM allocated in both pairs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t kColS = 256, kColQ = 384;
+  constexpr uint32_t kColS = 256, kColQ = 256 + 64 * NS;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1082,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
       const uint32_t lead_q = mapa_shared(smem_u32(q_full), lead_rank);
       if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QSBytes));
       const int qrow = grp * a.G * a.C + qt * kAttnBM;
-      for (int c = 0; c < 4; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, (4 + c) * 64, qrow);
+      for (int c = 0; c < 8 - K::QT; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, (K::QT + c) * 64, qrow);
       int it = 0;
       bool alive = true;
       auto acquire = [&]() -> uint8_t* {
@@ -1127,11 +1136,12 @@ __global__ void __launch_bounds__(kThreads4, 1)
             tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, pp * 256 + h * 128 + c * 64, row);
         }
       };
+      // the MMA warp's order: K 0 .. NS-1, then V n followed by K n+NS
+      for (int n = 0; n < NS && n < nb && alive; ++n) load_k(n);
       for (int n = 0; n < nb && alive; ++n) {
-        load_k(n);
-        if (n >= 1) load_v(n - 1);
+        load_v(n);
+        if (n + NS < nb && alive) load_k(n + NS);
       }
-      if (nb >= 1 && alive) load_v(nb - 1);
       if (leader) {
         volatile int no_abort = 0;
         mbar_wait(q_full, 0, &no_abort);
@@ -1157,53 +1167,59 @@ __global__ void __launch_bounds__(kThreads4, 1)
         ++it;
         return smem_u32(ring + s * kStageBytes);
       };
+      // descriptors advance by (byte offset >> 4) in their start-address
+      // field, so each MMA adds a constant to a base computed once
+      const uint64_t q_desc0 = smem_desc_sw128(q_base, 16, 1024);
       auto qk = [&](int n) {
-        const uint32_t tS = tmem + kColS + (n & 1) * 64;
+        const uint32_t tS = tmem + kColS + (n % NS) * 64;
         const uint32_t st = consume();
         if (!alive) return;
+        const uint64_t b_desc0 = smem_desc_sw128(st, 16, 1024);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = smem_desc_sw128(st + ch * 4096 + kk * 32, 16, 1024);
+            const uint64_t bd = b_desc0 + uint64_t((ch * 4096 + kk * 32) >> 4);
             const uint32_t acc = (ch | kk) != 0 ? 1u : 0u;
-            if (ch < 4) {
+            if (ch < K::QT)
               mma2_bf16_ts(tS, tmem + kColQ + ch * 32 + kk * 8, bd, idesc_qk, acc);
-            } else {
-              const uint64_t ad = smem_desc_sw128(q_base + (ch - 4) * 16384 + kk * 32, 16, 1024);
-              mma2_bf16_ss(tS, ad, bd, idesc_qk, acc);
-            }
+            else
+              mma2_bf16_ss(tS, q_desc0 + uint64_t(((ch - K::QT) * 16384 + kk * 32) >> 4), bd, idesc_qk, acc);
           }
         }
         mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
-        mma2_commit_mc(&s_full[n & 1], pair_mask);
+        mma2_commit_mc(&s_full[n % NS], pair_mask);
       };
+      const uint64_t po_desc0 = smem_desc_sw128(smem_u32(sPO), 16, 1024);
       auto pv = [&](int n) {
-        const uint32_t tS = tmem + kColS + (n & 1) * 64;
+        const uint32_t tS = tmem + kColS + (n % NS) * 64;
         const uint32_t st = consume();
         if (!alive) return;
-        const uint32_t po = smem_u32(sPO + (n & 1) * K::POBytes);
+        const uint64_t v_desc0 = smem_desc_sw128(st, 16384, 1024);
+        const uint64_t a_desc0 = po_desc0 + uint64_t(((n & 1) * K::POBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = smem_desc_sw128(st + pp * 8192 + kk * 2048, 16384, 1024);
-          mma2_bf16_ts(tmem, tS + kk * 8, bd, idesc_pv, (n | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          mma2_bf16_ts(tmem, tS + kk * 8, v_desc0 + uint64_t((pp * 8192 + kk * 2048) >> 4), idesc_pv,
+                       (n | kk) != 0 ? 1u : 0u);
+        // the other pair's keys once its P has landed in both CTAs
+        if (!mbar_wait(&px_full[n % NS], (n / NS) & 1, flags)) {
+          alive = false;
+          return;
         }
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = smem_desc_sw128(po + kk * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(st + (1 - pp) * 8192 + kk * 2048, 16384, 1024);
-          mma2_bf16_ss(tmem, ad, bd, idesc_pv, 1u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma2_bf16_ss(tmem, a_desc0 + uint64_t((kk * 32) >> 4),
+                       v_desc0 + uint64_t(((1 - pp) * 8192 + kk * 2048) >> 4), idesc_pv, 1u);
         mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
         mma2_commit_mc(&pv_done[n & 1], 0xF);
       };
-      if (alive && nb >= 1) qk(0);
-      if (alive && nb >= 2) qk(1);
+      for (int n = 0; n < NS && n < nb && alive; ++n) qk(n);
       for (int n = 0; n < nb && alive; ++n) {
-        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, flags)) break;
+        if (!mbar_wait(&p_full[n % NS], (n / NS) & 1, flags)) break;
         tc_fence_after();
         pv(n);
-        if (n + 2 < nb) qk(n + 2);
+        if (n + NS < nb) qk(n + NS);
       }
       // every MMA has completed in both CTAs of the pair before either releases TMEM
       mma2_commit_mc(drain, pair_mask);
@@ -1224,16 +1240,17 @@ __global__ void __launch_bounds__(kThreads4, 1)
     const int lo_row = valid ? window_lo(a, sq.P, i) : 0;
     const bool counter = warp == 2 && lane == 0;  // posts this CTA's expected exchange bytes
     // remote addresses; the second barrier of each pair sits 8 bytes after the first
-    const uint32_t lead_p0 = mapa_shared(smem_u32(&p_full[0]), lead_rank);
+    const uint32_t lead_p0 = mapa_shared(smem_u32(&p_full[0]), lead_rank);    // [NS]
+    const uint32_t lead_px0 = mapa_shared(smem_u32(&px_full[0]), lead_rank);  // [NS]
     const uint32_t peer_mx0 = mapa_shared(smem_u32(&mx_full[0]), partner);
     const uint32_t peer_po0 = mapa_shared(smem_u32(&po_full[0]), partner);
     const uint32_t peer_xin = mapa_shared(smem_u32(xin), partner);
     const uint32_t peer_sPO = mapa_shared(smem_u32(sPO), partner);
-    // Q d 0..255 of this row into TMEM (zeros past the last row of the group)
+    // the first QT chunks of this row's Q into TMEM (zeros past the last row of the group)
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.Qp + ((size_t)grp * GC + (valid ? R : 0)) * D);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < K::QT; ++ch) {
         uint32_t w[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -1259,12 +1276,13 @@ __global__ void __launch_bounds__(kThreads4, 1)
         mbar_arrive_expect_tx(&mx_full[buf], 4u * kAttnBM);
         mbar_arrive_expect_tx(&po_full[buf], uint32_t(K::POBytes));
       }
-      if (!mbar_wait(&s_full[buf], ph, flags)) {
+      const int sbuf = n % NS;
+      if (!mbar_wait(&s_full[sbuf], (n / NS) & 1, flags)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + kColS + buf * 64;
+      const uint32_t tS = tmem + lane_off + kColS + sbuf * 64;
       const int sb = 2 * (sq.kb0 + n) + pp;
       int pos0, hi_off = 64;
       if (sb < sq.n_pre) {
@@ -1284,9 +1302,16 @@ __global__ void __launch_bounds__(kThreads4, 1)
         for (int off = 0; off < 64; ++off)
           if (off < lo_off || off >= hi_off) sv[off] = __float_as_uint(-INFINITY);
       }
-      float smax = __uint_as_float(sv[0]);
+      float mx[16];
 #pragma unroll
-      for (int c = 1; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
+      for (int c = 0; c < 16; ++c)
+        mx[c] = fmaxf(fmaxf(__uint_as_float(sv[c]), __uint_as_float(sv[c + 16])),
+                      fmaxf(__uint_as_float(sv[c + 32]), __uint_as_float(sv[c + 48])));
+#pragma unroll
+      for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+      float smax = mx[0];
       // the two key halves agree on the block maximum (rounded up to bf16)
       const uint32_t mine = bf16_bits_up(smax);
       st_async_b32(peer_xin + uint32_t((buf * kAttnBM + lrow) * 4), mine, peer_mx0 + 8u * buf);
@@ -1307,6 +1332,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // P = 2^(S c - m) rounded to bf16, and its row sum (the normaliser
+      // matches what P.V consumes)
       uint32_t pk[32];
       float l_lo = 0.f, l_hi = 0.f;
 #pragma unroll
@@ -1365,6 +1392,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
       }
       tmem_st_wait();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(lead_p0 + 8u * sbuf);  // P.V over this pair's keys
       // the partner's P has landed in this CTA's shared memory
       if (!mbar_wait(&po_full[buf], ph, flags)) {
         alive = false;
@@ -1372,7 +1401,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(lead_p0 + 8u * buf);  // the pair leader issues P.V
+      if (lane == 0) mbar_arrive_remote(lead_px0 + 8u * sbuf);  // P.V over the other pair's keys
     }
     if (alive && nb >= 1) {
       alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
@@ -1441,12 +1470,16 @@ __global__ void __launch_bounds__(kThreads4, 1)
   }
 }
 
-// One block of 128 threads per output row (b, KV head, packed row g*C + i):
-// merges the KV splits' partial rows by their running max and sum.
-__global__ void __launch_bounds__(128) attention_combine_kernel(AttnTcArgs a) {
+// One warp per output row (b, KV head, packed row g*C + i), eight rows per
+// block: merges the KV splits' partial rows by their running max and sum,
+// four consecutive columns per lane and step (16-byte loads).
+__global__ void __launch_bounds__(256) attention_combine_kernel(AttnTcArgs a) {
   const int GC = a.G * a.C;
-  const int row = blockIdx.x % GC;
-  const int grp = blockIdx.x / GC;
+  const int lane = threadIdx.x & 31;
+  const long long wrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wrow >= (long long)a.B * a.Hkv * GC) return;
+  const int row = int(wrow % GC);
+  const int grp = int(wrow / GC);
   const int b = grp / a.Hkv, hk = grp % a.Hkv;
   const int g = row / a.C, i = row % a.C;
   const size_t rows_per_split = (size_t)a.B * a.Hkv * a.q_tiles * kAttnBM;
@@ -1461,19 +1494,21 @@ __global__ void __launch_bounds__(128) attention_combine_kernel(AttnTcArgs a) {
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int h = hk * a.G + g;
   __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d;
-  for (int c = threadIdx.x * 2; c < a.d; c += 256) {
-    float o0 = 0.f, o1 = 0.f;
+  for (int c = lane * 4; c < a.d; c += 128) {
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < a.nsplit; ++s) {
       const float ms = a.part_ml[(s * rows_per_split + prow0) * 2];
       if (ms == -INFINITY) continue;
       const float w = exp2f(ms - M);
-      const float2 v = *reinterpret_cast<const float2*>(a.part_o + (s * rows_per_split + prow0) * a.d + c);
-      o0 = fmaf(w, v.x, o0);
-      o1 = fmaf(w, v.y, o1);
+      const float4 v = *reinterpret_cast<const float4*>(a.part_o + (s * rows_per_split + prow0) * a.d + c);
+      o[0] = fmaf(w, v.x, o[0]);
+      o[1] = fmaf(w, v.y, o[1]);
+      o[2] = fmaf(w, v.z, o[2]);
+      o[3] = fmaf(w, v.w, o[3]);
     }
-    *reinterpret_cast<__nv_bfloat162*>(dst + c) = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    *reinterpret_cast<uint2*>(dst + c) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
   }
-  if (threadIdx.x == 0 && a.lse != nullptr)
+  if (lane == 0 && a.lse != nullptr)
     a.lse[((size_t)b * a.C + i) * a.Hq + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
@@ -1519,11 +1554,15 @@ cudaError_t launch_pair(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_
   return e;
 }
 
+#ifndef CANVAS_QUAD_S_BUFFERS
+#define CANVAS_QUAD_S_BUFFERS 2
+#endif
 cudaError_t launch_quad(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
+  constexpr int NS = CANVAS_QUAD_S_BUFFERS;
   static bool attr_set = false;
-  const int smem = Cfg4::Smem;
+  const int smem = Cfg4<NS>::Smem;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(attention_tc4_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1540,7 +1579,7 @@ cudaError_t launch_quad(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc4_kernel, maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc4_kernel<NS>, maps, a);
   count_launches(1);
   return e;
 }
@@ -1569,8 +1608,8 @@ cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cud
 }
 
 cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream) {
-  const int grid = a.B * a.Hkv * a.G * a.C;
-  attention_combine_kernel<<<grid, 128, 0, stream>>>(a);
+  const long long rows = (long long)a.B * a.Hkv * a.G * a.C;
+  attention_combine_kernel<<<int((rows + 7) / 8), 256, 0, stream>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }

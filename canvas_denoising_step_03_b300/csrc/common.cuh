@@ -397,8 +397,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // Ogita-Rump-Oishi), so g_hi + g_lo carries about 46 correct bits without any
 // fp64 arithmetic.  pos * g_hi = t + e exactly (two-product again),
 // t - rint(t) is exact, so the fraction of a turn f carries an absolute error
-// near 2^-25 for every pos < 2^24; sincospif then evaluates sin / cos of
-// 2*pi*f.
+// near 2^-25 for every pos < 2^24.  sin / cos of 2*pi*f (|2 pi f| <= pi) come
+// from the special-function unit (__sincosf: absolute error about 2^-21.4 on
+// [-pi, pi]); a rotated value is then off by about 5e-7 of its pair's
+// magnitude, far below the bf16 spacing it is rounded to.
 struct RopeTurns {
   float hi, lo;
 };
@@ -415,7 +417,7 @@ __device__ __forceinline__ void rope_cos_sin(int pos, RopeTurns g, float* c, flo
   const float t = __fmul_rn(p, g.hi);  // kept apart from the FMAs below
   const float e = fmaf(p, g.hi, -t);
   const float f = (t - rintf(t)) + (e + p * g.lo);
-  sincospif(2.0f * f, s, c);
+  __sincosf(6.28318530717958648f * f, s, c);
 }
 
 }  // namespace canvas

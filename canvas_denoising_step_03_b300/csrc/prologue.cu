@@ -298,20 +298,55 @@ __device__ __forceinline__ void key_prep_row(const KeyPrepArgs& k, int w, int ro
   }
 }
 
-// One warp per (b, KV head, row), grid-stride over the rows.  Rows
-// [0, max_prefix) (global layers only): prepared prefix keys Kt and value
-// scalars for positions below P64.  Rows [max_prefix, max_prefix + Tpad):
-// tail row t = row - max_prefix -- prefix rows P64 + t < P are gathered from
-// the cache, rows past the canvas are zeroed, canvas rows are left to the
-// prologue kernel.
+// Global layers, prefix rows below P64: four consecutive positions per warp
+// (one block-table lookup, the four rows' loads in flight together), each
+// written as its prepared key to Kt with its value scalar.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) key_prep_kernel(KeyPrepArgs k) {
-  const int row0 = k.global ? 0 : k.max_prefix;
-  const int L = k.max_prefix + k.Tpad - row0;
-  const int total = k.B * k.Hkv * L;
+__device__ __forceinline__ void key_prep_prefix4(const KeyPrepArgs& k, int w, int G4) {
+  const int lane = threadIdx.x & 31;
+  const int g4 = w % G4;
+  const int hk = (w / G4) % k.Hkv;
+  const int b = w / (G4 * k.Hkv);
+  const int P = k.prefix_len[b];
+  if (P < 0 || P > k.max_prefix) return;  // reported by the tail pass
+  const int pos0 = 4 * g4;
+  if (pos0 >= (P & ~63)) return;  // P64 is a multiple of 4: a group is all prefix or all past it
+  const int lp = pos0 / k.page_tokens, off = pos0 % k.page_tokens;  // the four rows share the page
+  const int page = (lp < k.max_pages) ? k.block_table[(size_t)b * k.max_pages + lp] : -1;
+  if (page < 0 || page >= k.num_pages) {
+    if (lane == 0) record_error(CANVAS_ERR_BOUNDS);
+    return;
+  }
+  const T* src = static_cast<const T*>(k.k_pool) + (((size_t)page * k.Hkv + hk) * k.page_tokens + off) * D;
+  Row r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) load_row<T, D>(src + j * D, r[j]);
+  const size_t orow = ((size_t)b * k.Hkv + hk) * k.max_prefix + pos0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    global_row<T, D>(r[j], k.gamma_k, k.eps, k.freq, pos0 + j, static_cast<T*>(k.Kt) + (orow + j) * D, nullptr,
+                     k.vs_pre + orow + j);
+}
+
+// Grid-stride over warps.  Global layers first prepare the prefix keys Kt
+// (four rows per warp, above).  Then one warp per tail row t = 0 .. Tpad-1
+// of every (b, KV head): prefix rows P64 + t < P are gathered from the cache
+// (global: prepared, raw values kept), rows past the canvas are zeroed,
+// canvas rows are left to the prologue kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(256, 2) key_prep_kernel(KeyPrepArgs k) {
   const int nwarps = int((gridDim.x * blockDim.x) >> 5);
-  for (int w = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5); w < total; w += nwarps)
-    key_prep_row<T, D>(k, w, row0, L);
+  const int w0 = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (k.global && k.page_tokens % 4 == 0) {
+    const int G4 = (k.max_prefix + 3) / 4;
+    const int total4 = k.B * k.Hkv * G4;
+    for (int w = w0; w < total4; w += nwarps) key_prep_prefix4<T, D>(k, w, G4);
+  } else if (k.global) {
+    const int totalp = k.B * k.Hkv * k.max_prefix;  // pages of other sizes: one row per warp
+    for (int w = w0; w < totalp; w += nwarps) key_prep_row<T, D>(k, w, 0, k.max_prefix);
+  }
+  const int total = k.B * k.Hkv * k.Tpad;
+  for (int w = w0; w < total; w += nwarps) key_prep_row<T, D>(k, w, k.max_prefix, k.Tpad);
 }
 
 template <typename T>
@@ -372,7 +407,7 @@ cudaError_t launch_prologue(const PrologueArgs& p, bool bf16, cudaStream_t strea
 }
 
 cudaError_t launch_key_prep(const KeyPrepArgs& k, bool bf16, cudaStream_t stream) {
-  const int rows = (k.global ? k.max_prefix : 0) + k.Tpad;
+  const int rows = (k.global ? (k.max_prefix + 3) / 4 : 0) + k.Tpad;
   const long long warps = (long long)k.B * k.Hkv * rows;
   const long long blocks = (warps * 32 + 255) / 256;
   count_launches(1);

@@ -19,6 +19,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <cstring>
+
 namespace canvas {
 
 namespace {
@@ -219,10 +221,29 @@ constexpr int kSmemSliceBytes = 65536;
 constexpr int kPieceElems = 8192;
 constexpr int kMaxPieces = kSmemSliceBytes / (2 * kPieceElems);
 
-template <int kThreads>
+__device__ __forceinline__ float bf16x2_max(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  __nv_bfloat162 x, y, z, w;
+  memcpy(&x, &a, 4);
+  memcpy(&y, &b, 4);
+  memcpy(&z, &c, 4);
+  memcpy(&w, &d, 4);
+  const __nv_bfloat162 m = __hmax2(__hmax2(x, y), __hmax2(z, w));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
+// The first pass is split in two: the thread's maximum and the 8-element
+// group holding it first (packed bf16 maxima, no exponentials), then Z and T
+// about that exact maximum -- no running rescale, no data-dependent branch
+// per group.  Thread t owns 16-byte chunks t + kThreads k of the slice (8
+// logits each, increasing with k), read conflict-free from shared memory.
+// kFull: the slice is exactly kSmemSliceBytes (compile-time trip counts).
+template <int kThreads, bool kFull>
 __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a,
                                                                      const __nv_bfloat16* __restrict__ logits) {
   constexpr int kWarps = kThreads / 32;
+  constexpr int kMaxK = kSmemSliceBytes / 16 / kThreads;           // chunks per thread
+  constexpr int kKPerPiece = kPieceElems / 8 / kThreads;            // of them in one bulk-copy piece
+  static_assert(kKPerPiece >= 1 && kMaxK % kKPerPiece == 0, "piece layout");
   extern __shared__ __align__(128) uint8_t slice_raw[];
   __shared__ RowState warp_part[kWarps];
   __shared__ __align__(16) uint32_t cl_msg[kMaxSampleCluster][8];
@@ -234,9 +255,10 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   const uint32_t csize = gridDim.x;
   const long long c0 = (long long)rank * a.chunk;
   const long long c1 = min((long long)a.V, c0 + a.chunk);
-  const int n = c1 > c0 ? int(c1 - c0) : 0;  // a multiple of 8
+  const int n = kFull ? kSmemSliceBytes / 2 : (c1 > c0 ? int(c1 - c0) : 0);  // a multiple of 8
+  const int nch = n / 8;
   const __nv_bfloat16* src = logits + (long long)row * a.V + c0;
-  const __nv_bfloat16* slice = reinterpret_cast<const __nv_bfloat16*>(slice_raw);
+  const uint4* slice4 = reinterpret_cast<const uint4*>(slice_raw);
   if (threadIdx.x == 0) {
     for (int p = 0; p < kMaxPieces; ++p) mbar_init(&full[p], 1);
     mbar_init(&red_bar, 1);
@@ -255,24 +277,62 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   // itself needs no memory ordering)
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   const float ysc = a.inv_temp * kLog2e;
-  RowState s;
-  state_init(s);
-  for (int p = 0; p * kPieceElems < n; ++p) {
+  // (1) the thread's maximum and the first chunk that holds it
+  float bv = -INFINITY;
+  int bk = -1;
+#pragma unroll
+  for (int k = 0; k < kMaxK; ++k) {
     // on a timeout the status word is set and the CTA carries on, so that
     // no peer waits for it
-    mbar_wait(&full[p], 0, &abort_flag);
-    const int e = min(n, (p + 1) * kPieceElems);
-    for (int i = p * kPieceElems + threadIdx.x * 8; i < e; i += kThreads * 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      float x[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[2 * j] = __uint_as_float(w[j] << 16);
-        x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    if (k % kKPerPiece == 0 && (k / kKPerPiece) * kPieceElems < n) mbar_wait(&full[k / kKPerPiece], 0, &abort_flag);
+    const int j = int(threadIdx.x) + k * kThreads;
+    if (kFull || j < nch) {
+      const uint4 u = slice4[j];
+      const float gm = bf16x2_max(u.x, u.y, u.z, u.w);
+      if (gm > bv) {  // strict: the earlier chunk keeps a tie
+        bv = gm;
+        bk = k;
       }
-      state_add8(s, x, ysc, int(c0) + i);
     }
+  }
+  RowState s;
+  state_init(s);
+  if (bk >= 0) {
+    const int jb = int(threadIdx.x) + bk * kThreads;
+    const uint4 u = slice4[jb];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    int e = 7;
+#pragma unroll
+    for (int q = 3; q >= 0; --q) {
+      if (__uint_as_float(w[q] & 0xffff0000u) == bv) e = 2 * q + 1;
+      if (__uint_as_float(w[q] << 16) == bv) e = 2 * q;
+    }
+    s.bx = bv;
+    s.bi = int(c0) + 8 * jb + e;
+    // (2) Z and T about the thread's maximum (base 2)
+    const float mt = bv * ysc;
+    float Z = 0.f, T = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < kMaxK; ++k) {
+      const int j = int(threadIdx.x) + k * kThreads;
+      if (kFull || j < nch) {
+        const uint4 v = slice4[j];
+        const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float t0 = fmaf(__uint_as_float(x4[q] << 16), ysc, -mt);
+          const float t1 = fmaf(__uint_as_float(x4[q] & 0xffff0000u), ysc, -mt);
+          const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+          Z += e0;
+          Z += e1;
+          T = fmaf(t0, e0, T);
+          T = fmaf(t1, e1, T);
+        }
+      }
+    }
+    s.m = mt;
+    s.Z = Z;
+    s.T = T;
   }
   // warp, then CTA, then cluster (every CTA merges the partial states in
   // rank order, so all end with the same bits)
@@ -327,8 +387,12 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   const RowState t = warp_part[0];  // m and 1 / Z
   const float M = t.m;
   const float invZ = t.Z;
-  for (int i = threadIdx.x * 8; i < n; i += kThreads * 8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(slice + i);
+#pragma unroll 4
+  for (int k = 0; k < kMaxK; ++k) {
+    const int j = int(threadIdx.x) + k * kThreads;
+    if (!kFull && j >= nch) break;
+    const int i = 8 * j;
+    const uint4 u = slice4[j];
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     float p[8];
 #pragma unroll
@@ -446,13 +510,19 @@ cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, c
   if (bf16 && size_t(a.chunk) * 2 <= size_t(kSmemSliceBytes)) {
     static bool attr_set = false;
     if (!attr_set) {
-      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemSliceBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemSliceBytes);
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
     cfg.dynamicSmemBytes = size_t(a.chunk) * 2;
-    e = cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads>, a, lb);
+    // every CTA's slice exactly full: compile-time trip counts
+    const bool full = size_t(a.chunk) * 2 == size_t(kSmemSliceBytes) && (long long)a.chunk * a.cluster == a.V;
+    e = full ? cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, true>, a, lb)
+             : cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, false>, a, lb);
   } else if (bf16) {
     e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<__nv_bfloat16, kThreads>, a, lb);
   } else {

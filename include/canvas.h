@@ -109,7 +109,7 @@ size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, i
  * the glossary entries on partial RoPE and sliding-window attention; window
  * 1,024 per [TC] "아키텍처".
  *
- *   x        [B, C, D]            canvas input, dtype (row-major)
+ *   x        [B, C, D]            canvas input, dtype (row-major), 16-byte aligned
  *   W_q      [Hq*d, D]            dtype;  q = x W_q^T
  *   W_k      [Hkv*d, D]           dtype;  k = x W_k^T
  *   W_v      [Hkv*d, D] or NULL   dtype;  NULL only on global layers (W_v = W_k)
@@ -131,7 +131,7 @@ size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, i
  *   v_unit_rms                    0 (default).  1 on a global layer: value =
  *                                 sqrt(d) * r / (||r|| + eps) (the scalar is
  *                                 applied in fp32 to each key's softmax weight)
- *   out      [B, C, Hq*d] dtype   heads concatenated, 'n l h -> l (n h)'
+ *   out      [B, C, Hq*d] dtype   heads concatenated, 'n l h -> l (n h)', 16-byte aligned
  *   lse      [B, C, Hq] fp32 or NULL   natural-log softmax normaliser
  *   workspace, ws_bytes           >= canvas_attention_workspace_size(...),
  *                                 256-byte aligned; contents are scratch

@@ -62,3 +62,18 @@ def test_host_validation_errors(cv):
     # workspace too small
     st = lib.canvas_gemm_bf16(fake, fake, 0, fake, 4, 8, 16, 0, fake, 16, None)
     assert st == cv.CANVAS_ERR_WORKSPACE
+
+
+def test_misaligned_buffers_are_rejected_before_any_device_work(cv):
+    lib = cv.lib
+    good, bad = ctypes.c_void_p(256), ctypes.c_void_p(264)
+    # GEMM entry points: A, B and C must be 16-byte aligned
+    assert lib.canvas_gemm_bf16(good, good, 0, bad, 4, 8, 16, 0, good, 1 << 20, None) == cv.CANVAS_ERR_ARG
+    assert "aligned" in cv.canvas_last_error()
+    assert lib.canvas_gemm_bf16_to_bf16(good, bad, 0, good, 4, 8, 16, good, 1 << 20, None) == cv.CANVAS_ERR_ARG
+    # attention: x and out
+    kv = cv.canvas_kv_cache()
+    st = lib.canvas_attention(good, cv.CANVAS_BF16, 1, 16, 128, good, good, None, 2, 1, 64, good, good, 1e-6,
+                              good, 1, ctypes.byref(kv), good, 0, 0, 1.0, 0, bad, None, good, 1 << 30, None)
+    assert st == cv.CANVAS_ERR_ARG
+    assert "aligned" in cv.canvas_last_error()

@@ -145,3 +145,27 @@ def test_full_vocab_workload(cv):
     ref["soft_emb"] = soft_full
     assert 0.3 < ref["commit_mask"].mean() < 0.7
     compare(cv, s, run, ref, soft_rows=soft_rows)
+
+
+@pytest.mark.parametrize("V", [262144, 262136])   # every slice full / a shorter last slice
+def test_argmax_ties_take_the_lowest_index(cv, V):
+    """Exact ties of the maximum inside one 8-logit group, across the threads
+    of a CTA and across the CTAs of a row's cluster: the lowest index wins."""
+    rows, D = 6, 8
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((rows, V)).astype(np.float32)
+    ties = [[5, 3000, 70000, V - 1], [V - 9, V - 1], [17, 19, 16], [33000, 32768 + 8, 65536 * 3 + 1],
+            [2048 * 3 + 7, 2048 * 3 + 6], [0, V - 1]]
+    for r, idx in enumerate(ties):
+        x[r, idx] = 9.0
+    bits = wl.f32_to_bf16_bits(x)
+    E = wl.f32_to_bf16_bits(rng.standard_normal((V, D)).astype(np.float32) * 0.02)
+    cfg = wl.SampleConfig("ties", rows=rows, C=rows, V=V, D=D, dtype="bf16", seed=3, step=0, bound=0.3,
+                          logits="normal", peak=0.0, gen_temperature=1.0, E_std=0.02)
+    s = wl.SampleInputs(cfg=cfg, logits=bits, E=E, peaked=np.zeros(rows, bool))
+    run = SampleRun(cv, s)
+    got = run.amax.cpu().numpy()
+    np.testing.assert_array_equal(got, [min(t) for t in ties])
+    ref = osamp.canvas_sample(wl.as_f64(bits, "bf16"), wl.as_f64(E, "bf16"), 0.3, 3, 0, canvas_len=rows,
+                              probs_storage="bf16")
+    np.testing.assert_array_equal(got, ref["argmax"])
