@@ -33,9 +33,11 @@
 //                The accumulator is rescaled only when the running max grows
 //                by more than 8 (P stays below 2^8), so most blocks never
 //                touch O.
-// With d = 512 the 128 x 512 fp32 accumulator would fill all of TMEM, so the
-// value dimension is split across two CTAs (DV = 256 each) that both form
-// the full S; every other shape keeps the whole row in one CTA.
+// With d = 512 the 128 x 512 fp32 accumulator would fill all of TMEM: the
+// four-SM kernel further below splits the value dimension and the key blocks
+// between two CTA pairs (this kernel can also split the value dimension
+// across two CTAs that both form the full S); every other shape keeps the
+// whole row in one CTA.
 // Results: bf16 rows (and the natural-log LSE) when the key range is not
 // split, else fp32 partial rows plus (max, sum) for the combine kernel.
 // Every mbarrier wait is bounded (common.cuh).
@@ -551,425 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// The 2-SM form (head_dim 256 and 512).  A cluster of two CTAs holds two
-// consecutive 128-row query tiles of the same (sequence, KV head, value part,
-// KV split); the leader (cluster rank 0) issues every MMA for both:
-//   S = Q K^T   M = 256 (each CTA its 128 rows of Q), N = 128 keys: CTA r
-//               holds keys 64 r .. 64 r + 63 of every block (its sub-block);
-//   O += P V    M = 256 (P from each CTA's TMEM), N = 256 value columns: CTA r
-//               holds value columns 128 r .. 128 r + 127 of all 128 keys.
-// Each SM thus receives half the K and V bytes per block that a single CTA
-// would, for the same MMA work.  Barriers: the leader's full / q_full count
-// the TMA bytes of both CTAs; the commits go to both CTAs (multicast); the
-// softmax warps of both CTAs arrive on the leader's p_full.
-template <int D>
-struct Cfg2 {
-  static constexpr int DV = 256;
-  static constexpr int NCH = D / 64;
-  static constexpr int KST = D / 256;           // K stages per block: 64 keys x 256 d = 32 KB
-  static constexpr int NST = D == 512 ? 3 : 5;
-  static constexpr int QBytes = NCH * 16384;
-  static constexpr int Smem = QBytes + NST * kStageBytes + 1024 + kBarBytes + kXchgBytes;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attention_tc2_kernel(const __grid_constant__ AttnTcMaps maps, AttnTcArgs a) {
-  using K = Cfg2<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* ring = smem + K::QBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + K::NST * kStageBytes);
-  uint64_t* empty = full + K::NST;
-  uint64_t* q_full = empty + K::NST;
-  uint64_t* s_full = q_full + 1;   // [2]
-  uint64_t* p_full = s_full + 2;   // [2]
-  uint64_t* pv_done = p_full + 2;  // [2]
-  uint64_t* drain = pv_done + 2;
-  uint64_t* xbar = drain + 1;      // [4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
-  static_assert((2 * K::NST + 1 + 2 * 3 + 1 + 4) * 8 + 8 <= kBarBytes, "barrier area");
-  uint16_t* xmax = reinterpret_cast<uint16_t*>(ring + K::NST * kStageBytes + kBarBytes);  // [2][2][128]
-  float* xsum = reinterpret_cast<float*>(xmax);                                          // [2][128]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  int x = blockIdx.x >> 1;  // the pair's unit
-  const int dvp = x % a.dv_parts;
-  x /= a.dv_parts;
-  const int q_pairs = (a.q_tiles + 1) / 2;
-  const int qp = x % q_pairs;
-  x /= q_pairs;
-  const int split = x % a.nsplit;
-  x /= a.nsplit;
-  const int hk = x % a.Hkv;
-  const int b = x / a.Hkv;
-  const int grp = b * a.Hkv + hk;
-  const int qt = 2 * qp + int(rank);
-  // identical in both CTAs: the pair's row range decides the key blocks
-  const Seq sq = make_seq(a, b, qp, split, 2 * kAttnBM);
-  if (!sq.ok) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(CANVAS_ERR_BOUNDS);
-    return;  // uniform over the pair: before any barrier, cluster barrier or TMEM allocation
-  }
-  const int nb = sq.nb;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < K::NST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(q_full, 1);
-    for (int j = 0; j < 2; ++j) {
-      mbar_init(&s_full[j], 1);
-      mbar_init(&p_full[j], 16);  // the eight softmax warps of both CTAs
-      mbar_init(&pv_done[j], 1);
-    }
-    mbar_init(drain, 1);
-    for (int j = 0; j < 4; ++j) mbar_init(&xbar[j], 2);
-    flags[0] = 0;
-    fence_mbarrier_init();
-    tma_prefetch_desc(&maps.q);
-    tma_prefetch_desc(&maps.kpre);
-    tma_prefetch_desc(&maps.vpre);
-    tma_prefetch_desc(&maps.kx);
-    tma_prefetch_desc(&maps.vx);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, 512);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer (both CTAs)
-      const uint32_t lead_q = mapa_shared(smem_u32(q_full), 0);
-      if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QBytes));
-      const int qrow = grp * a.G * a.C + qt * kAttnBM;
-      for (int c = 0; c < K::NCH; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, c * 64, qrow);
-      int it = 0;
-      bool alive = true;
-      auto acquire = [&]() -> uint8_t* {
-        const int s = it % K::NST;
-        if (!mbar_wait(&empty[s], ((it / K::NST) & 1) ^ 1, flags)) {
-          alive = false;
-          return nullptr;
-        }
-        if (leader) mbar_arrive_expect_tx(&full[s], uint32_t(2 * kStageBytes));
-        ++it;
-        return ring + s * kStageBytes;
-      };
-      auto lead_full = [&]() { return mapa_shared(smem_u32(&full[(it - 1) % K::NST]), 0); };
-      auto row_of = [&](int sb, bool key, const CUtensorMap*& map) -> int {
-        if (sb < sq.n_pre) {
-          const int pos = sq.s0 + 64 * sb;
-          map = key ? &maps.kpre : &maps.vpre;
-          return (key && !a.kpre_paged) ? grp * a.max_prefix + pos : paged_row(a, b, hk, pos);
-        }
-        map = key ? &maps.kx : &maps.vx;
-        return grp * a.Tpad + 64 * (sb - sq.n_pre);
-      };
-      auto load_k = [&](int n) {
-        // this CTA's 64 keys of block n, all of d: KST stages of 4 d-chunks
-        const int sb = 2 * (sq.kb0 + n) + int(rank);
-        for (int ks = 0; ks < K::KST && alive; ++ks) {
-          uint8_t* dst = acquire();
-          if (!dst) break;
-          const CUtensorMap* map;
-          const int row = row_of(sb, true, map);
-          const uint32_t bar = lead_full();
-          for (int c = 0; c < 4; ++c) tma_load_2d_pair(dst + c * 8192, map, bar, (ks * 4 + c) * 64, row);
-        }
-      };
-      auto load_v = [&](int n) {
-        // all 128 keys of block n, this CTA's 128 value columns
-        if (!alive) return;
-        uint8_t* dst = acquire();
-        if (!dst) return;
-        const uint32_t bar = lead_full();
-        for (int u = 0; u < 2; ++u) {
-          const CUtensorMap* map;
-          const int row = row_of(2 * (sq.kb0 + n) + u, false, map);
-          for (int c = 0; c < 2; ++c)
-            tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, dvp * K::DV + int(rank) * 128 + c * 64, row);
-        }
-      };
-      for (int n = 0; n < nb && alive; ++n) {
-        load_k(n);
-        if (n >= 1) load_v(n - 1);
-      }
-      if (nb >= 1 && alive) load_v(nb - 1);
-      // drain (leader): every stage's bytes -- both CTAs' -- have landed
-      if (leader) {
-        volatile int no_abort = 0;
-        mbar_wait(q_full, 0, &no_abort);
-        for (int j = max(0, it - K::NST); j < it; ++j) mbar_wait(&full[j % K::NST], (j / K::NST) & 1, &no_abort);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ------------------------------------------------ MMA issuer (leader)
-      const uint32_t idesc_qk = idesc_bf16_f32(256, kAttnBN, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16_f32(256, K::DV, 0, 1);
-      const uint32_t q_base = smem_u32(sQ);
-      int it = 0;
-      bool alive = mbar_wait(q_full, 0, flags);
-      tc_fence_after();
-      auto consume = [&]() -> uint32_t {
-        const int s = it % K::NST;
-        if (!mbar_wait(&full[s], (it / K::NST) & 1, flags)) {
-          alive = false;
-          return 0;
-        }
-        tc_fence_after();
-        ++it;
-        return smem_u32(ring + s * kStageBytes);
-      };
-      auto qk = [&](int n) {
-        const uint32_t tS = tmem + 256 + (n & 1) * 128;
-        for (int ks = 0; ks < K::KST && alive; ++ks) {
-          const uint32_t st = consume();
-          if (!alive) return;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int ch = ks * 4 + c;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(q_base + ch * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(st + c * 8192 + kk * 32, 16, 1024);
-              mma2_bf16_ss(tS, ad, bd, idesc_qk, (ch | kk) != 0 ? 1u : 0u);
-            }
-          }
-          mma2_commit_mc(&empty[(it - 1) % K::NST], 3);
-        }
-        mma2_commit_mc(&s_full[n & 1], 3);
-      };
-      auto pv = [&](int n) {
-        const uint32_t tS = tmem + 256 + (n & 1) * 128;
-        const uint32_t st = consume();
-        if (!alive) return;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = smem_desc_sw128(st + kk * 2048, 16384, 1024);
-          mma2_bf16_ts(tmem, tS + kk * 8, bd, idesc_pv, (n | kk) != 0 ? 1u : 0u);
-        }
-        mma2_commit_mc(&empty[(it - 1) % K::NST], 3);
-        mma2_commit_mc(&pv_done[n & 1], 3);
-      };
-      if (alive && nb >= 1) qk(0);
-      if (alive && nb >= 2) qk(1);
-      for (int n = 0; n < nb && alive; ++n) {
-        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, flags)) break;
-        tc_fence_after();
-        pv(n);
-        if (n + 2 < nb) qk(n + 2);
-      }
-      // every MMA has completed in both CTAs before either releases TMEM
-      mma2_commit_mc(drain, 3);
-    }
-    if (lane == 0) {
-      volatile int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort);
-    }
-  } else {
-    // ------------------------------------------------ softmax + epilogue (both CTAs)
-    const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int lrow = quad * 32 + lane;
-    const uint32_t lane_off = uint32_t(quad * 32) << 16;
-    const int GC = a.G * a.C;
-    const int R = qt * kAttnBM + lrow;
-    const bool valid = R < GC;
-    const int g = valid ? R / a.C : 0, i = valid ? R % a.C : 0;
-    const int lo_row = valid ? window_lo(a, sq.P, i) : 0;
-    constexpr int DVH = K::DV / 2;
-    const uint32_t lead_p[2] = {mapa_shared(smem_u32(&p_full[0]), 0), mapa_shared(smem_u32(&p_full[1]), 0)};
-    float m_run = -INFINITY, l = 0.f;
-    bool alive = true;
-    int xphase = 0;
-    auto pair_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[quad]);
-      const bool ok = mbar_wait(&xbar[quad], uint32_t(xphase & 1), flags);
-      ++xphase;
-      return ok;
-    };
-    for (int n = 0; n < nb; ++n) {
-      if (!mbar_wait(&s_full[n & 1], (n >> 1) & 1, flags)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tS = tmem + lane_off + 256 + (n & 1) * 128;
-      const int kb = sq.kb0 + n;
-      const int sb = 2 * kb + half;
-      int pos0, hi_off = 64;
-      if (sb < sq.n_pre) {
-        pos0 = sq.s0 + 64 * sb;
-      } else {
-        const int t0 = 64 * (sb - sq.n_pre);
-        pos0 = sq.P64 + t0;
-        hi_off = min(64, sq.T - t0);
-      }
-      const int lo_off = max(0, lo_row - pos0);
-      uint32_t sv[64];
-      tmem_ld32(tS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
-      if (__any_sync(0xffffffffu, lo_off > 0 || hi_off < 64)) {
-#pragma unroll
-        for (int off = 0; off < 64; ++off)
-          if (off < lo_off || off >= hi_off) sv[off] = __float_as_uint(-INFINITY);
-      }
-      float smax = __uint_as_float(sv[0]);
-#pragma unroll
-      for (int c = 1; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sv[c]));
-      const uint16_t mine = bf16_bits_up(smax);
-      xmax[((n & 1) * 2 + half) * kAttnBM + lrow] = mine;
-      if (!pair_sync()) {
-        alive = false;
-        break;
-      }
-      const uint16_t other = xmax[((n & 1) * 2 + (half ^ 1)) * kAttnBM + lrow];
-      smax = fmaxf(bf16_bits_to_f32(mine), bf16_bits_to_f32(other));
-      const float bmax = smax * a.c_log2;
-      const float m_new = fmaxf(m_run, bmax);
-      const bool need = (m_run != -INFINITY) && (m_new > m_run + kRescaleLog2);
-      const float alpha = need ? exp2f(m_run - m_new) : 1.f;
-      if (need) {
-        l *= alpha;
-        m_run = m_new;
-      } else if (m_run == -INFINITY) {
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float l_lo = 0.f, l_hi = 0.f;
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c = c2 * 32 + 2 * j;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), a.c_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), a.c_log2, -m_use));
-          if (a.vs_pre == nullptr) {
-            pk[j] = pack_bf16x2(p0, p1);
-            l_lo += __uint_as_float(pk[j] << 16);
-            l_hi += __uint_as_float(pk[j] & 0xffff0000u);
-          } else {
-            float sc[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int off = c + e;
-              sc[e] = sb < sq.n_pre ? a.vs_pre[(size_t)grp * a.max_prefix + pos0 + off]
-                                    : a.vs_tail[(size_t)grp * a.Tpad + (pos0 - sq.P64) + off];
-            }
-            pk[j] = pack_bf16x2(p0 * sc[0], p1 * sc[1]);
-            const float w0 = __uint_as_float(pk[j] << 16), w1 = __uint_as_float(pk[j] & 0xffff0000u);
-            l_lo += sc[0] > 0.f ? w0 / sc[0] : 0.f;
-            l_hi += sc[1] > 0.f ? w1 / sc[1] : 0.f;
-          }
-        }
-        tmem_st16(tS + half * 32 + c2 * 16, pk);
-      }
-      l += l_lo + l_hi;
-      if (__any_sync(0xffffffffu, need)) {
-        if (!mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < DVH / 32; ++cc) {
-          uint32_t r[32];
-          const uint32_t col = uint32_t(half * DVH + cc * 32);
-          tmem_ld32(tmem + lane_off + col, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(tmem + lane_off + col, r);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(lead_p[n & 1]);  // the leader issues P.V
-    }
-    if (alive && nb >= 1) {
-      alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
-      tc_fence_after();
-    }
-    float l_row = l;
-    if (alive) alive = pair_sync();
-    if (alive) {
-      xsum[half * kAttnBM + lrow] = l;
-      alive = pair_sync();
-      l_row = l + xsum[(half ^ 1) * kAttnBM + lrow];
-    }
-    if (alive) {
-      const int h = hk * a.G + g;
-      if (a.nsplit == 1) {
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d + dvp * K::DV + half * DVH;
-        for (int cc = 0; cc < DVH / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + uint32_t(half * DVH + cc * 32), r);
-          tmem_ld_wait();
-          if (valid) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
-            uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          }
-        }
-        if (valid && dvp == 0 && half == 0 && a.lse != nullptr)
-          a.lse[((size_t)b * a.C + i) * a.Hq + h] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
-      } else {
-        const size_t prow = ((size_t)split * a.B * a.Hkv + grp) * (size_t)(a.q_tiles * kAttnBM) + qt * kAttnBM + lrow;
-        if (qt < a.q_tiles) {
-          float* dst = a.part_o + prow * a.d + dvp * K::DV + half * DVH;
-          for (int cc = 0; cc < DVH / 32; ++cc) {
-            uint32_t r[32];
-            if (nb >= 1) {
-              tmem_ld32(tmem + lane_off + uint32_t(half * DVH + cc * 32), r);
-              tmem_ld_wait();
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = 0u;
-            }
-            float4* o4 = reinterpret_cast<float4*>(dst + cc * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              o4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          }
-          if (dvp == 0 && half == 0) {
-            a.part_ml[prow * 2] = m_run;
-            a.part_ml[prow * 2 + 1] = l_row;
-          }
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  cluster_sync_all();  // both CTAs done with TMEM, the leader's drain seen in both
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -1527,33 +1110,6 @@ cudaError_t launch_d(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t s
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_pair(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
-  static bool attr_set = false;
-  const int smem = Cfg2<D>::Smem;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int pairs = a.B * a.Hkv * a.nsplit * ((a.q_tiles + 1) / 2) * a.dv_parts;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc2_kernel<D>, maps, a);
-  count_launches(1);
-  return e;
-}
-
 #ifndef CANVAS_QUAD_S_BUFFERS
 #define CANVAS_QUAD_S_BUFFERS 2
 #endif
@@ -1600,9 +1156,8 @@ cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cud
   switch (a.d) {
     case 64: return launch_d<64>(maps, a, stream);
     case 128: return launch_d<128>(maps, a, stream);
-    case 256: return a.pair ? launch_pair<256>(maps, a, stream) : launch_d<256>(maps, a, stream);
-    case 512: return a.pair == 2 ? launch_quad(maps, a, stream)
-                                 : a.pair ? launch_pair<512>(maps, a, stream) : launch_d<512>(maps, a, stream);
+    case 256: return launch_d<256>(maps, a, stream);
+    case 512: return a.pair == 2 ? launch_quad(maps, a, stream) : launch_d<512>(maps, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

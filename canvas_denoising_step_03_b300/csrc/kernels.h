@@ -150,8 +150,8 @@ constexpr int kAttnBN = 128;       // keys per block
 struct AttnTcArgs {
   int B, C, Hq, Hkv, G, d, DV, dv_parts, q_tiles, nsplit, max_prefix, window, Tpad;
   int kpre_paged;            // 1: prefix keys from the paged pool; 0: dense Kt
-  int pair;                  // 1: 2-SM kernel (CTA pairs share each MMA), head_dim 256 / 512;
-                             // 2: 4-SM kernel (two pairs split the key blocks), head_dim 512
+  int pair;                  // 2: 4-SM kernel (two CTA pairs split the key blocks), head_dim 512;
+                             // 0: one SM per 128-row tile
   const __nv_bfloat16* Qp;   // [B][Hkv][G][C][d] prepared queries (the 4-SM kernel reads half of each row)
   const int32_t* block_table;
   int max_pages, page_tokens, num_pages;
