@@ -573,6 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (d 0..127) sits in TMEM and the ring has three stages; with two, half of Q
 // sits in TMEM and the ring has four stages (two blocks of K and V in flight).
 // TMEM columns: O [0, 256), S / P NS x 64 from 256, Q at 256 + 64 NS.
+// The ring is split in two: NST - 1 stages of K, loaded by warp 0 in block
+// order, and one stage of V, loaded by warp 6 -- so the keys of the next
+// blocks' S are fetched as soon as an S has consumed its stage, without
+// queueing behind the values of the current block.
 template <int NS>
 struct Cfg4 {
   static constexpr int NST = NS == 2 ? 4 : 3;
@@ -581,7 +585,7 @@ struct Cfg4 {
   static constexpr int POBytes = 16384;      // the partner's P: 128 rows x 64 keys bf16
   static constexpr int Smem = QSBytes + 2 * POBytes + NST * kStageBytes + 1024 + kBarBytes + 1024;
 };
-constexpr int kThreads4 = 192;  // TMA warp, MMA warp, 4 softmax / epilogue warps
+constexpr int kThreads4 = 224;  // K TMA warp, MMA warp, 4 softmax / epilogue warps, V TMA warp
 
 template <int NS>
 __global__ void __launch_bounds__(kThreads4, 1)
@@ -668,67 +672,54 @@ __global__ void __launch_bounds__(kThreads4, 1)
   const uint32_t tmem = *tmem_slot;
   constexpr uint32_t kColS = 256, kColQ = 256 + 64 * NS;
 
-  if (warp == 0) {
+  constexpr int KR = K::NST - 1;  // K stages [0, KR), the V stage KR
+  auto row_of = [&](int sb, bool key, const CUtensorMap*& map) -> int {
+    if (sb < sq.n_pre) {
+      const int pos = sq.s0 + 64 * sb;
+      map = key ? &maps.kpre32 : &maps.vpre;
+      return (key && !a.kpre_paged) ? grp * a.max_prefix + pos : paged_row(a, b, hk, pos);
+    }
+    map = key ? &maps.kx32 : &maps.vx;
+    return grp * a.Tpad + 64 * (sb - sq.n_pre);
+  };
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer (every CTA)
-      const uint32_t lead_q = mapa_shared(smem_u32(q_full), lead_rank);
-      if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QSBytes));
-      const int qrow = grp * a.G * a.C + qt * kAttnBM;
-      for (int c = 0; c < 8 - K::QT; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, (K::QT + c) * 64, qrow);
-      int it = 0;
-      bool alive = true;
-      auto acquire = [&]() -> uint8_t* {
-        const int s = it % K::NST;
-        if (!mbar_wait(&empty[s], ((it / K::NST) & 1) ^ 1, flags)) {
-          alive = false;
-          return nullptr;
-        }
+      // ------------------------------------------------ TMA producers (every CTA): K (warp 0), V (warp 6)
+      const bool kp = warp == 0;
+      const int nst = kp ? KR : 1, s0 = kp ? 0 : KR;
+      if (kp) {
+        const uint32_t lead_q = mapa_shared(smem_u32(q_full), lead_rank);
+        if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QSBytes));
+        const int qrow = grp * a.G * a.C + qt * kAttnBM;
+        for (int c = 0; c < 8 - K::QT; ++c) tma_load_2d_pair(sQ + c * 16384, &maps.q, lead_q, (K::QT + c) * 64, qrow);
+      }
+      int n = 0;
+      for (; n < nb; ++n) {
+        const int s = s0 + n % nst;
+        if (!mbar_wait(&empty[s], ((n / nst) & 1) ^ 1, flags)) break;
         if (leader) mbar_arrive_expect_tx(&full[s], uint32_t(2 * kStageBytes));
-        ++it;
-        return ring + s * kStageBytes;
-      };
-      auto lead_full = [&]() { return mapa_shared(smem_u32(&full[(it - 1) % K::NST]), lead_rank); };
-      auto row_of = [&](int sb, bool key, const CUtensorMap*& map) -> int {
-        if (sb < sq.n_pre) {
-          const int pos = sq.s0 + 64 * sb;
-          map = key ? &maps.kpre32 : &maps.vpre;
-          return (key && !a.kpre_paged) ? grp * a.max_prefix + pos : paged_row(a, b, hk, pos);
-        }
-        map = key ? &maps.kx32 : &maps.vx;
-        return grp * a.Tpad + 64 * (sb - sq.n_pre);
-      };
-      auto load_k = [&](int n) {
-        // this CTA's 32 keys of the pair's key half, all of d: 8 chunks of 4 KB
-        uint8_t* dst = acquire();
-        if (!dst) return;
-        const CUtensorMap* map;
-        const int row = row_of(2 * (sq.kb0 + n) + pp, true, map) + 32 * h;
-        const uint32_t bar = lead_full();
-        for (int c = 0; c < 8; ++c) tma_load_2d_pair(dst + c * 4096, map, bar, c * 64, row);
-      };
-      auto load_v = [&](int n) {
-        // all 128 keys of block n, this CTA's 128 columns of value half pp
-        if (!alive) return;
-        uint8_t* dst = acquire();
-        if (!dst) return;
-        const uint32_t bar = lead_full();
-        for (int u = 0; u < 2; ++u) {
+        uint8_t* dst = ring + s * kStageBytes;
+        const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead_rank);
+        if (kp) {
+          // this CTA's 32 keys of the pair's key half, all of d: 8 chunks of 4 KB
           const CUtensorMap* map;
-          const int row = row_of(2 * (sq.kb0 + n) + u, false, map);
-          for (int c = 0; c < 2; ++c)
-            tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, pp * 256 + h * 128 + c * 64, row);
+          const int row = row_of(2 * (sq.kb0 + n) + pp, true, map) + 32 * h;
+          for (int c = 0; c < 8; ++c) tma_load_2d_pair(dst + c * 4096, map, bar, c * 64, row);
+        } else {
+          // all 128 keys of block n, this CTA's 128 columns of value half pp
+          for (int u = 0; u < 2; ++u) {
+            const CUtensorMap* map;
+            const int row = row_of(2 * (sq.kb0 + n) + u, false, map);
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, pp * 256 + h * 128 + c * 64, row);
+          }
         }
-      };
-      // the MMA warp's order: K 0 .. NS-1, then V n followed by K n+NS
-      for (int n = 0; n < NS && n < nb && alive; ++n) load_k(n);
-      for (int n = 0; n < nb && alive; ++n) {
-        load_v(n);
-        if (n + NS < nb && alive) load_k(n + NS);
       }
       if (leader) {
+        // drain: every stage's bytes -- both CTAs' -- have landed
         volatile int no_abort = 0;
-        mbar_wait(q_full, 0, &no_abort);
-        for (int j = max(0, it - K::NST); j < it; ++j) mbar_wait(&full[j % K::NST], (j / K::NST) & 1, &no_abort);
+        if (kp) mbar_wait(q_full, 0, &no_abort);
+        for (int j = max(0, n - nst); j < n; ++j) mbar_wait(&full[s0 + j % nst], (j / nst) & 1, &no_abort);
       }
     }
   } else if (warp == 1) {
@@ -737,17 +728,17 @@ __global__ void __launch_bounds__(kThreads4, 1)
       const uint32_t idesc_qk = idesc_bf16_f32(256, 64, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(256, 256, 0, 1);
       const uint32_t q_base = smem_u32(sQ);
-      int it = 0;
       bool alive = mbar_wait(q_full, 0, flags) && mbar_wait(qt_ready, 0, flags);
       tc_fence_after();
-      auto consume = [&]() -> uint32_t {
-        const int s = it % K::NST;
-        if (!mbar_wait(&full[s], (it / K::NST) & 1, flags)) {
+      // K of block n: stage n % KR; V of block n: stage KR
+      auto consume = [&](int n, bool key) -> uint32_t {
+        const int s = key ? n % KR : KR;
+        const uint32_t par = key ? (n / KR) & 1 : n & 1;
+        if (!mbar_wait(&full[s], par, flags)) {
           alive = false;
           return 0;
         }
         tc_fence_after();
-        ++it;
         return smem_u32(ring + s * kStageBytes);
       };
       // descriptors advance by (byte offset >> 4) in their start-address
@@ -755,7 +746,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
       const uint64_t q_desc0 = smem_desc_sw128(q_base, 16, 1024);
       auto qk = [&](int n) {
         const uint32_t tS = tmem + kColS + (n % NS) * 64;
-        const uint32_t st = consume();
+        const uint32_t st = consume(n, true);
         if (!alive) return;
         const uint64_t b_desc0 = smem_desc_sw128(st, 16, 1024);
 #pragma unroll
@@ -770,13 +761,13 @@ __global__ void __launch_bounds__(kThreads4, 1)
               mma2_bf16_ss(tS, q_desc0 + uint64_t(((ch - K::QT) * 16384 + kk * 32) >> 4), bd, idesc_qk, acc);
           }
         }
-        mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
+        mma2_commit_mc(&empty[n % KR], pair_mask);
         mma2_commit_mc(&s_full[n % NS], pair_mask);
       };
       const uint64_t po_desc0 = smem_desc_sw128(smem_u32(sPO), 16, 1024);
       auto pv = [&](int n) {
         const uint32_t tS = tmem + kColS + (n % NS) * 64;
-        const uint32_t st = consume();
+        const uint32_t st = consume(n, false);
         if (!alive) return;
         const uint64_t v_desc0 = smem_desc_sw128(st, 16384, 1024);
         const uint64_t a_desc0 = po_desc0 + uint64_t(((n & 1) * K::POBytes) >> 4);
@@ -794,7 +785,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma2_bf16_ss(tmem, a_desc0 + uint64_t((kk * 32) >> 4),
                        v_desc0 + uint64_t(((1 - pp) * 8192 + kk * 2048) >> 4), idesc_pv, 1u);
-        mma2_commit_mc(&empty[(it - 1) % K::NST], pair_mask);
+        mma2_commit_mc(&empty[KR], pair_mask);
         mma2_commit_mc(&pv_done[n & 1], 0xF);
       };
       for (int n = 0; n < NS && n < nb && alive; ++n) qk(n);

@@ -197,6 +197,51 @@ __device__ __forceinline__ void global_row(Row& r, const float* gamma_k, float e
   store_row<T, D>(kdst, r);
 }
 
+// Four stored raw rows r[j] at positions pos0 + j (global layers): their keys
+// rotate(rms(r[j])) to kdst + j D and value scalars to vs[j].  The same
+// arithmetic as global_row, element by element, with each QK-norm weight,
+// frequency and turn split loaded or formed once for the four rows and one
+// norm per row.
+template <typename T, int D>
+__device__ __forceinline__ void global_rows4(Row (&r)[4], const float* gamma, float eps, const float* freq, int pos0,
+                                             T* kdst, float* vs) {
+  using S = RowShape<D>;
+  constexpr int np = S::np, half = S::half;
+  const int lane = threadIdx.x & 31;
+  float scale[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    scale[j] = sqrtf(float(D)) / (row_norm<D>(r[j]) + eps);
+    if (lane == 0) vs[j] = scale[j];
+  }
+#pragma unroll
+  for (int k = 0; k < np; ++k) {
+    const int t = S::elem(lane, k);
+    const float g_lo = gamma[t], g_hi = gamma[t + half];
+    const float f = freq[t];
+    if (f != 0.f) {
+      const RopeTurns tw = rope_turns(f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = g_lo * r[j].lo[k] * scale[j];
+        const float b = g_hi * r[j].hi[k] * scale[j];
+        float c, sn;
+        rope_cos_sin(pos0 + j, tw, &c, &sn);
+        r[j].lo[k] = c * a - sn * b;
+        r[j].hi[k] = c * b + sn * a;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        r[j].lo[k] = g_lo * r[j].lo[k] * scale[j];
+        r[j].hi[k] = g_hi * r[j].hi[k] * scale[j];
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) store_row<T, D>(kdst + j * D, r[j]);
+}
+
 // One warp per (canvas token, head).  Heads: Hq query heads, then Hkv key
 // heads, then (sliding) Hkv value heads.
 template <typename T, int D>
@@ -322,10 +367,7 @@ __device__ __forceinline__ void key_prep_prefix4(const KeyPrepArgs& k, int w, in
 #pragma unroll
   for (int j = 0; j < 4; ++j) load_row<T, D>(src + j * D, r[j]);
   const size_t orow = ((size_t)b * k.Hkv + hk) * k.max_prefix + pos0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    global_row<T, D>(r[j], k.gamma_k, k.eps, k.freq, pos0 + j, static_cast<T*>(k.Kt) + (orow + j) * D, nullptr,
-                     k.vs_pre + orow + j);
+  global_rows4<T, D>(r, k.gamma_k, k.eps, k.freq, pos0, static_cast<T*>(k.Kt) + orow * D, k.vs_pre + orow);
 }
 
 // Grid-stride over warps.  Global layers first prepare the prefix keys Kt
