@@ -1,15 +1,16 @@
 // sampler.cu -- the per-position vocab sampler of a denoising step.
 //
 // One thread-block cluster per canvas position (row).  Each CTA of the
-// cluster owns a contiguous slice of the vocabulary, streams it once with
-// 16-byte loads and keeps an online (max, sum, entropy-sum) state plus the
-// argmax; the CTAs swap their partial states through distributed shared
-// memory and every CTA merges them in rank order (so all agree bit for bit).
-// CTA 0 then writes the row's entropy / confidence / argmax and the
-// commit-or-renoise decision; every CTA writes the probabilities of its
-// slice.  bf16 logits: each thread holds its part of the slice in registers
-// (up to 16 x 16 bytes, all loads in flight at once), so the logits are read
-// from HBM exactly once.  fp32 logits (small vocabularies) re-read the slice.
+// cluster owns a contiguous slice of the vocabulary and reduces it to a
+// (max, sum, entropy-sum) state plus the argmax; the CTAs swap their partial
+// states through distributed shared memory and every CTA merges them in rank
+// order (so all agree bit for bit).  CTA 0 then writes the row's entropy /
+// confidence / argmax and the commit-or-renoise decision; every CTA writes
+// the probabilities of its slice.  bf16 logits with slices up to 64 KB: the
+// slice is staged in shared memory by bulk copies, so the logits are read
+// from HBM exactly once (sample_rows_smem_kernel).  Otherwise (fp32 logits,
+// larger slices) the slice is streamed from global memory twice, with an
+// online state (sample_rows_kernel).
 //
 // Method: AI Trends summary of a DiffusionGemma 26B notebook
 // (aitrends.kr/articles/94089), "섹션별 상세", sampling-loop paragraph (entropy
