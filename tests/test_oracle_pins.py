@@ -204,11 +204,14 @@ def test_single_key_returns_its_value_row_and_gqa_mapping():
         np.testing.assert_allclose(out[0, 0, h * 16:(h + 1) * 16], v[hk * 16:(hk + 1) * 16], rtol=1e-13)
 
 
-def _sdpa_reference(inp):
+def _sdpa_reference(inp, scale=1.0, v_unit_rms=False, with_lse=False):
     """The attention core through torch's scaled_dot_product_attention (fp64)
     with an explicit boolean mask, fed with q/k/v assembled from the pinned
-    rms / rotate building blocks."""
+    rms / rotate building blocks; the natural-log softmax normaliser of each
+    row from scipy's logsumexp over the same masked scores."""
+    from scipy.special import logsumexp
     c = inp.cfg
+    lses = []
     x, Wq, Wk = _f64(inp, "x"), _f64(inp, "W_q"), _f64(inp, "W_k")
     Wv = _f64(inp, "W_v")
     outs = []
@@ -225,6 +228,8 @@ def _sdpa_reference(inp):
             r = np.concatenate([_f64(inp, "cache_k")[b, :, :P], k], 1)
             K = onum.rotate(onum.rms(r, inp.gamma_k, c.eps), inp.freq, 0)
             Vv = r
+            if v_unit_rms:   # sqrt(d) r / (|r| + eps), no weight
+                Vv = math.sqrt(c.d) * r / (np.linalg.norm(r, axis=-1, keepdims=True) + c.eps)
         mask = np.ones((c.C, P + c.C), bool)
         if c.layer == "sliding" and c.window > 0:
             for i in range(c.C):
@@ -234,8 +239,12 @@ def _sdpa_reference(inp):
         Vq = np.repeat(Vv, G, axis=0)
         o = torch.nn.functional.scaled_dot_product_attention(
             torch.from_numpy(q), torch.from_numpy(Kq), torch.from_numpy(Vq),
-            attn_mask=torch.from_numpy(mask), scale=1.0).numpy()
+            attn_mask=torch.from_numpy(mask), scale=scale).numpy()
         outs.append(o.transpose(1, 0, 2).reshape(c.C, c.Hq * c.d))
+        sc = np.einsum("hid,hjd->hij", q, Kq) * scale
+        lses.append(logsumexp(np.where(mask[None], sc, -np.inf), axis=-1).T)   # [C, Hq]
+    if with_lse:
+        return np.stack(outs), np.stack(lses)
     return np.stack(outs)
 
 
@@ -246,6 +255,22 @@ def test_attention_matches_library_sdpa(layer, window, rot):
     inp = wl.make_attention_inputs(cfg)
     out, _ = _run_oracle(inp)
     np.testing.assert_allclose(out, _sdpa_reference(inp), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("layer,scale,unit", [("sliding", 0.37, False), ("global", 1.0, True), ("global", 2.5, True)])
+def test_scale_unit_rms_values_and_lse_match_library_sdpa(layer, scale, unit):
+    """The softmax scale argument, the unit-RMS value variant of global layers
+    and the natural-log normaliser the oracle returns, against the library
+    path (SDPA) and scipy's logsumexp."""
+    cfg = _small_cfg(layer=layer, window=16 if layer == "sliding" else 0, gamma_q=None, gamma_k=None,
+                     rotary_fraction=0.25 if layer == "global" else 1.0, theta=1e6 if layer == "global" else 1e4)
+    inp = wl.make_attention_inputs(cfg)
+    out, lse = _run_oracle(inp, scale=scale, v_unit_rms=unit)
+    want, want_lse = _sdpa_reference(inp, scale=scale, v_unit_rms=unit, with_lse=True)
+    np.testing.assert_allclose(out, want, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, rtol=1e-12, atol=1e-12)
+    if unit:   # the variant changes the result
+        assert np.max(np.abs(out - _run_oracle(inp, scale=scale)[0])) > 1e-3
 
 
 def test_global_storage_model_decomposition():
