@@ -10,7 +10,9 @@
  *   canvas_sample    -- the per-position vocab sampler: softmax, entropy,
  *                       argmax, confidence, entropy-bound commit / uniform
  *                       renoise, and the self-conditioning soft embedding P.E.
- * plus a bf16 GEMM used by callers that assemble whole layers around them.
+ * plus the glue a caller needs to assemble whole denoising steps around them:
+ * bf16 GEMMs (fp32 or bf16 output), the canvas input embedding and an
+ * fp32 -> bf16 cast.
  *
  * Sources (the method is described on web pages, cited by title and section):
  *   [AIT] AI Trends summary of a DiffusionGemma 26B weights notebook
@@ -163,7 +165,7 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  * glossary entry of [AIT] (expected embedding P.E of the softmax).
  *
  *   logits   [rows, V] dtype      rows = B*C positions; 16-byte aligned
- *   E        [V, D] dtype         embedding table (row-major)
+ *   E        [V, D] dtype         embedding table (row-major), 16-byte aligned
  *   entropy_bound                 commit iff entropy < bound (nats, strict)
  *   seed, step                    renoise key = m(m(m(seed) ^ step) ^ row),
  *                                 m = one SplitMix64 output; token = key mod V
@@ -180,8 +182,9 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  *   argmax   [rows] int32 or NULL out: lowest index of the largest logit
  *   probs_out [rows, V] or NULL   out: softmax, in probs_dtype; 16-byte aligned
  *   probs_dtype                   CANVAS_BF16 or CANVAS_FP32
- *   soft_emb [rows, D] fp32       out: P.E.  bf16 calls multiply the bf16
- *                                 probabilities; fp32 calls the fp32 ones.
+ *   soft_emb [rows, D] fp32       out: P.E, 16-byte aligned.  bf16 calls
+ *                                 multiply the bf16 probabilities; fp32 calls
+ *                                 the fp32 ones.
  *   workspace, ws_bytes           >= canvas_sample_workspace_size(...)
  *
  * Supported: V % 8 == 0, D % 8 == 0, rows >= 1.
