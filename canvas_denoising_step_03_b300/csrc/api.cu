@@ -719,8 +719,9 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
   if (probs_out && probs_dtype != CANVAS_BF16 && probs_dtype != CANVAS_FP32)
     return fail(CANVAS_ERR_ARG, "canvas_sample: probs_dtype");
   if (V % 8 != 0 || D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_sample: V and D must be multiples of 8");
-  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs_out)) % 16 != 0)
-    return fail(CANVAS_ERR_ARG, "canvas_sample: logits and probs_out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs_out) | reinterpret_cast<uintptr_t>(E) |
+       reinterpret_cast<uintptr_t>(soft_emb)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_sample: logits, probs_out, E and soft_emb must be 16-byte aligned");
   const SampleLayout L = sample_layout(dtype, rows, V, D);
   if (!ws_ok(workspace, ws_bytes, L.total))
     return fail(CANVAS_ERR_WORKSPACE, "canvas_sample: workspace missing, small or misaligned (need %zu)", L.total);

@@ -77,3 +77,8 @@ def test_misaligned_buffers_are_rejected_before_any_device_work(cv):
                               good, 1, ctypes.byref(kv), good, 0, 0, 1.0, 0, bad, None, good, 1 << 30, None)
     assert st == cv.CANVAS_ERR_ARG
     assert "aligned" in cv.canvas_last_error()
+    # sampler: logits, probs_out, E and soft_emb
+    st = lib.canvas_sample(good, cv.CANVAS_BF16, 4, 512, bad, 64, 0.3, 0, 0, 1.0, 0, 4, None, None, good, good,
+                           good, good, None, None, cv.CANVAS_BF16, good, good, 1 << 30, None)
+    assert st == cv.CANVAS_ERR_ARG
+    assert "aligned" in cv.canvas_last_error()
