@@ -520,42 +520,6 @@ def load_traffic(kernel: str):
 
 
 # --------------------------------------------------------------------------- oracle timings
-def oracle_step_sample(a_in, s_in, attn_rows, samp_rows, E64_chunks=16384):
-    """Time the fp64 oracle on a bounded sample of one step; returns (extrapolated
-    seconds per full step, description)."""
-    from oracle import attention as oatt
-    from oracle import sampler as osamp
-    c = a_in.cfg
-    f = lambda x: None if x is None else wl.as_f64(x, c.dtype)  # noqa: E731
-    t0 = time.perf_counter()
-    oatt.canvas_attention(f(a_in.x), f(a_in.W_q), f(a_in.W_k), None, c.Hq, c.Hkv, c.d,
-                          a_in.gamma_q.astype(np.float64), a_in.gamma_k.astype(np.float64), c.eps,
-                          a_in.freq.astype(np.float64), c.layer, f(a_in.cache_k), None, a_in.prefix_len, c.window,
-                          storage="bf16", rows=[(0, 0, 0)])
-    t_fixed = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oatt.canvas_attention(f(a_in.x), f(a_in.W_q), f(a_in.W_k), None, c.Hq, c.Hkv, c.d,
-                          a_in.gamma_q.astype(np.float64), a_in.gamma_k.astype(np.float64), c.eps,
-                          a_in.freq.astype(np.float64), c.layer, f(a_in.cache_k), None, a_in.prefix_len, c.window,
-                          storage="bf16", rows=attn_rows)
-    t_rows = time.perf_counter() - t0 - t_fixed
-    per_row = max(t_rows, 0.0) / max(1, len(attn_rows) - 0)
-    sc = s_in.cfg
-    t0 = time.perf_counter()
-    lg = wl.as_f64(s_in.logits[samp_rows], "bf16")
-    res = osamp.canvas_sample(lg, None, sc.bound, sc.seed, 0, canvas_len=sc.C, probs_storage="bf16")
-    soft = np.zeros((len(samp_rows), sc.D))
-    for v0 in range(0, sc.V, E64_chunks):
-        soft += res["probs"][:, v0:v0 + E64_chunks] @ wl.as_f64(s_in.E[v0:v0 + E64_chunks], "bf16")
-    t_samp = time.perf_counter() - t0
-    total_rows = c.B * c.C * c.Hq
-    t_full = t_fixed + per_row * total_rows + t_samp / len(samp_rows) * sc.rows
-    desc = (f"fp64 numpy oracle: attention fixed part (projections, all key transforms) + {len(attn_rows)} of "
-            f"{total_rows} query rows, sampler + soft embedding for {len(samp_rows)} of {sc.rows} positions; "
-            f"full step extrapolated linearly in rows")
-    return t_full, desc, t_fixed + t_rows + t_samp
-
-
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -566,27 +530,105 @@ def blas_threads():
 
 
 def cpu_baseline(a_in, s_in):
-    attn_rows = [(0, h, i) for h in (0, 9) for i in (0, 255)]
-    t_full, desc, spent = oracle_step_sample(a_in, s_in, attn_rows, [0, 1])
-    return {"value": round(1.0 / t_full, 6), "unit": "canvas steps/s", "cores": blas_threads(),
-            "kind": "oracle", "sample": desc, "cpu_seconds_spent": round(spent, 2),
+    """The oracle's whole step, extrapolated from one timing of every piece
+    (OracleClock), on this host's cores."""
+    clock = OracleClock(a_in, s_in)
+    t0 = time.perf_counter()
+    for i, piece in enumerate(clock.pieces):
+        clock.run(piece, i)
+    spent = time.perf_counter() - t0
+    return {"value": round(1.0 / clock.estimate(), 6), "unit": "canvas steps/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": clock.describe(rotating=False), "cpu_seconds_spent": round(spent, 2),
             "host_cpus": len(os.sched_getaffinity(0))}
+
+
+class OracleClock:
+    """Times the fp64 oracle's step in bounded pieces and extrapolates the
+    whole step from the latest time of each piece: the attention call for one
+    query row (it includes the projections and every key transform) and for
+    1 + R rows (the difference is R rows' cost), the sampler statistics and
+    decision of one position, and that position's soft embedding over one
+    16384-entry slice of E.  Inputs are converted to fp64 outside every
+    timed piece; only the oracle's own arithmetic is timed."""
+
+    CHUNK = 16384
+    R = 16
+
+    def __init__(self, a_in, s_in):
+        c = a_in.cfg
+        f = lambda x: None if x is None else wl.as_f64(x, c.dtype)  # noqa: E731
+        self.a_in, self.s_in, self.c, self.sc = a_in, s_in, c, s_in.cfg
+        self.args = (f(a_in.x), f(a_in.W_q), f(a_in.W_k), f(a_in.W_v), c.Hq, c.Hkv, c.d,
+                     a_in.gamma_q.astype(np.float64), a_in.gamma_k.astype(np.float64), c.eps,
+                     a_in.freq.astype(np.float64), c.layer, f(a_in.cache_k), f(a_in.cache_v), a_in.prefix_len, c.window)
+        self.n_chunks = (self.sc.V + self.CHUNK - 1) // self.CHUNK
+        self.t = {}
+        self.probs = None
+        self.pieces = ["attn1", "attnR", "stats"] + [f"chunk{j}" for j in range(self.n_chunks)]
+
+    def _rows(self, k, n):
+        return [(0, (k + j) % self.c.Hq, (37 * (k + j)) % self.c.C) for j in range(n)]
+
+    def run(self, piece, k):
+        """Run one piece (k picks the rows / position); returns its seconds."""
+        from oracle import attention as oatt
+        from oracle import sampler as osamp
+        if piece.startswith("attn"):
+            rows = self._rows(k, 1 if piece == "attn1" else 1 + self.R)
+            t0 = time.perf_counter()
+            oatt.canvas_attention(*self.args, storage=self.c.dtype if self.c.dtype == "bf16" else "fp64", rows=rows)
+            dt = time.perf_counter() - t0
+        elif piece == "stats":
+            lg = wl.as_f64(self.s_in.logits[[k % self.sc.rows]], self.sc.dtype)
+            t0 = time.perf_counter()
+            res = osamp.canvas_sample(lg, None, self.sc.bound, self.sc.seed, 0, canvas_len=self.sc.C,
+                                      probs_storage="bf16" if self.sc.dtype == "bf16" else "fp64")
+            dt = time.perf_counter() - t0
+            self.probs = res["probs"]
+        else:
+            if self.probs is None:
+                self.run("stats", k)
+            v0 = int(piece[5:]) * self.CHUNK
+            E64 = wl.as_f64(self.s_in.E[v0:v0 + self.CHUNK], self.sc.dtype)
+            t0 = time.perf_counter()
+            _ = self.probs[:, v0:v0 + self.CHUNK] @ E64
+            dt = time.perf_counter() - t0
+        self.t[piece] = dt
+        return dt
+
+    def estimate(self):
+        """Seconds of one whole step from the latest piece times."""
+        per_row = max(self.t["attnR"] - self.t["attn1"], 0.0) / self.R
+        fixed = max(self.t["attn1"] - per_row, 0.0)
+        rows = self.c.B * self.c.C * self.c.Hq
+        per_pos = self.t["stats"] + sum(self.t[f"chunk{j}"] for j in range(self.n_chunks))
+        return fixed + per_row * rows + per_pos * self.sc.rows
+
+    def describe(self, rotating=True):
+        how = "one piece per step in rotation" if rotating else "every piece once"
+        return (f"fp64 numpy oracle timed in pieces ({how}): attention with 1 and "
+                f"{1 + self.R} query rows (projections and every key transform included), the sampler of one "
+                f"position, its soft embedding over one of {self.n_chunks} slices of E; whole step extrapolated "
+                f"linearly in query rows ({self.c.B * self.c.C * self.c.Hq}) and positions ({self.sc.rows}) from "
+                f"the latest time of every piece")
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    a_in = wl.make_attention_inputs(wl.GLOBAL)
-    s_in = wl.make_sample_inputs(wl.FULL_SAMPLE)
+    clock = OracleClock(wl.make_attention_inputs(wl.GLOBAL), wl.make_sample_inputs(wl.FULL_SAMPLE))
+    for i, piece in enumerate(clock.pieces):  # every piece measured once before the first estimate
+        clock.run(piece, i)
+    npieces = len(clock.pieces)
     times = []
-    desc = ""
     for k in range(args.warmup + args.steps):
-        t_full, desc, _ = oracle_step_sample(a_in, s_in, [(0, k % 16, (37 * k) % 256)], [k % 256])
+        clock.run(clock.pieces[k % npieces], k)
         if k >= args.warmup:
-            times.append(t_full)
+            times.append(clock.estimate())
     ms = statistics.mean(times) * 1000.0
     v = round(1000.0 / ms, 6)
     cores = blas_threads()
+    desc = clock.describe()
     return {"metric": METRIC, "value": v, "unit": "canvas steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded draws)", "impl": "reference",

@@ -58,3 +58,26 @@ def test_reference_arm_reports_on_rank_zero_only():
     class Args:
         steps, warmup = 1, 0
     assert bench.run_reference(Args(), rank=1, world=2) is None
+
+
+def test_oracle_clock_times_every_piece_and_extrapolates():
+    """The reference arm's clock on a small global layer and sampler: every
+    piece gets a time, the estimate is positive and grows with the rows it
+    extrapolates to."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import canvas_workloads as wl
+    a = wl.make_attention_inputs(wl.AttnConfig("clk", B=1, C=8, prefix=(40,), D=64, Hq=2, Hkv=1, d=64,
+                                               layer="global", window=0, theta=1e6, rotary_fraction=0.25,
+                                               dtype="bf16", seed=1, page_tokens=64))
+    s = wl.make_sample_inputs(wl.SampleConfig("clk", rows=4, C=4, V=40000, D=16, dtype="bf16", seed=2, step=0,
+                                              bound=0.3, logits="normal"))
+    clock = bench.OracleClock(a, s)
+    assert clock.n_chunks == 3 and len(clock.pieces) == 6
+    for i, piece in enumerate(clock.pieces):
+        assert clock.run(piece, i) >= 0.0
+    est = clock.estimate()
+    assert est > 0.0
+    clock.t["stats"] += 1.0       # one more second per position: 4 positions
+    assert abs(clock.estimate() - est - 4.0) < 1e-9
+    assert "rotation" in clock.describe() and "every piece once" in clock.describe(rotating=False)
