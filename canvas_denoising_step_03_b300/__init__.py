@@ -38,7 +38,7 @@ EXPORTED = [
     "canvas_attention_workspace_size", "canvas_attention", "canvas_sample_workspace_size", "canvas_sample",
     "canvas_gemm_workspace_size", "canvas_gemm_bf16", "canvas_last_error", "canvas_device_status",
     "canvas_version", "canvas_profile_events", "canvas_kernel_launches", "canvas_gemm_bf16_noalloc",
-    "canvas_embed_input", "canvas_cast_bf16", "canvas_gemm_bf16_to_bf16",
+    "canvas_embed_input", "canvas_cast_bf16", "canvas_gemm_bf16_to_bf16", "canvas_selftest_wait_timeout",
 ]
 
 # size of the static scratch behind canvas_gemm_bf16_noalloc (include/canvas.h)
@@ -81,6 +81,8 @@ def _load(path: str = LIB_PATH):
     lib.canvas_gemm_workspace_size.restype = Z
     lib.canvas_gemm_bf16.argtypes = [P, P, I, P, I, I, I, I, P, Z, P]
     lib.canvas_gemm_bf16.restype = I
+    lib.canvas_selftest_wait_timeout.argtypes = [P]
+    lib.canvas_selftest_wait_timeout.restype = I
     lib.canvas_gemm_bf16_to_bf16.argtypes = [P, P, I, P, I, I, I, P, Z, P]
     lib.canvas_gemm_bf16_to_bf16.restype = I
     lib.canvas_gemm_bf16_noalloc.argtypes = [P, P, I, P, I, I, I, I, P]
@@ -210,6 +212,11 @@ def canvas_gemm_bf16_to_bf16(A, B, b_layout, C, workspace, stream=None):
     N = B.shape[0] if b_layout == 0 else B.shape[1]
     _check(lib.canvas_gemm_bf16_to_bf16(_ptr(A), _ptr(B), int(b_layout), _ptr(C), M, N, K, _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def canvas_selftest_wait_timeout(stream=None):
+    """Enqueue the diagnostic kernel whose bounded wait runs out (include/canvas.h)."""
+    _check(lib.canvas_selftest_wait_timeout(_stream(stream)))
 
 
 def canvas_gemm_bf16_noalloc(A, B, b_layout, C, accumulate, stream=None):

@@ -368,6 +368,11 @@ canvas_status canvas_device_status(canvas_stream_t stream) {
   return CANVAS_OK;
 }
 
+canvas_status canvas_selftest_wait_timeout(canvas_stream_t stream) {
+  CANVAS_CUDA(launch_wait_timeout_selftest(reinterpret_cast<cudaStream_t>(stream)));
+  return CANVAS_OK;
+}
+
 size_t canvas_gemm_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 1) return 0;
   return gemm_ws_bytes(plan_gemm(M, N, K)) + kAlign;

@@ -1,7 +1,8 @@
 // glue.cu -- the two element-wise kernels a caller needs to chain canvas
 // steps into a multi-layer denoising loop: the canvas input (embedding of the
 // current tokens plus the self-conditioning soft embedding of the previous
-// step) and a round-to-bf16 cast of fp32 activations.
+// step) and a round-to-bf16 cast of fp32 activations; and a diagnostic kernel
+// that exercises the bounded-wait timeout path of every pipelined kernel.
 //
 // Self-conditioning: the expected embedding P.E of the previous step's
 // softmax is added to the canvas input (AI Trends summary of a DiffusionGemma
@@ -65,6 +66,21 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float4* __restrict
   }
 }
 
+// One thread waits, through the same bounded wait as every pipelined kernel,
+// on an mbarrier phase that nothing completes: after the wait limit it
+// records CANVAS_ERR_TIMEOUT in the status word and the kernel returns.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag);
+}
+
 }  // namespace
 
 cudaError_t launch_embed_input(const int32_t* tokens, const void* E, const float* soft, int rows, int D, int V,
@@ -81,6 +97,12 @@ cudaError_t launch_cast_bf16(const float* in, void* out, long long n, cudaStream
   const long long n8 = n / 8;
   const int blocks = int(std::min<long long>((n8 + 255) / 256, 148LL * 16));
   cast_bf16_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>();
   count_launches(1);
   return cudaGetLastError();
 }

@@ -176,5 +176,6 @@ cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream);
 cudaError_t launch_embed_input(const int32_t* tokens, const void* E, const float* soft, int rows, int D, int V,
                                void* x, float* x32, cudaStream_t stream);
 cudaError_t launch_cast_bf16(const float* in, void* out, long long n, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
 
 }  // namespace canvas

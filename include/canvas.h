@@ -261,6 +261,18 @@ canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const flo
 canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stream_t stream);
 
 /*
+ * canvas_selftest_wait_timeout -- diagnostic; the method has no counterpart.
+ *
+ * Enqueues one kernel whose bounded device wait can never complete (an
+ * mbarrier phase that nothing finishes), the same wait every pipelined kernel
+ * of this library uses.  After the wait limit (2 s) the kernel records
+ * CANVAS_ERR_TIMEOUT in the per-device status word and returns: the next
+ * canvas_device_status() reports it (and clears it), and the context stays
+ * usable.  Asynchronous on `stream`; CANVAS_ERR_CUDA if the launch fails.
+ */
+canvas_status canvas_selftest_wait_timeout(canvas_stream_t stream);
+
+/*
  * canvas_gemm_bf16_noalloc -- canvas_gemm_bf16 without a caller workspace.
  *
  * The pages have no counterpart to this call; it exists for callers that
