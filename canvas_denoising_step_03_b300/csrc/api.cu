@@ -444,6 +444,10 @@ canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layou
     return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: b_layout must be 0 or 1");
   if (K % 8 != 0 || N % 8 != 0)
     return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gemm_bf16_noalloc: K and N must be multiples of 8");
+  // C goes straight to the vectorised split reduce when K is split, so it is
+  // checked here like A and B, before anything is enqueued
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: A, B and C must be 16-byte aligned");
   const size_t need = canvas_gemm_workspace_size(M, N, K);
   if (need > CANVAS_GEMM_NOALLOC_SCRATCH_BYTES)
     return fail(CANVAS_ERR_WORKSPACE,

@@ -294,7 +294,11 @@ canvas_status canvas_selftest_wait_timeout(canvas_stream_t stream);
  * device current); make that first call before any stream capture.  All
  * calls share the one array: calls that may overlap on the GPU (different
  * streams, or different host threads, without ordering between them) race
- * on it and must be serialised by the caller.
+ * on it and must be serialised by the caller.  The looked-up address is kept
+ * for the life of the process: do not use this call on a device after
+ * cudaDeviceReset() (the library's module, and the array with it, may be
+ * loaded again at another address).  A, B and C must be 16-byte aligned
+ * (CANVAS_ERR_ARG otherwise, before anything is enqueued).
  */
 #define CANVAS_GEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
 canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layout, float* C,

@@ -71,6 +71,11 @@ def test_misaligned_buffers_are_rejected_before_any_device_work(cv):
     assert lib.canvas_gemm_bf16(good, good, 0, bad, 4, 8, 16, 0, good, 1 << 20, None) == cv.CANVAS_ERR_ARG
     assert "aligned" in cv.canvas_last_error()
     assert lib.canvas_gemm_bf16_to_bf16(good, bad, 0, good, 4, 8, 16, good, 1 << 20, None) == cv.CANVAS_ERR_ARG
+    # the no-workspace GEMM: a C that is 4-byte but not 16-byte aligned (a
+    # column-offset view) is rejected before the scratch lookup or any launch
+    assert lib.canvas_gemm_bf16_noalloc(good, good, 0, ctypes.c_void_p(260), 128, 256, 4096, 0,
+                                        None) == cv.CANVAS_ERR_ARG
+    assert "aligned" in cv.canvas_last_error()
     # attention: x and out
     kv = cv.canvas_kv_cache()
     st = lib.canvas_attention(good, cv.CANVAS_BF16, 1, 16, 128, good, good, None, 2, 1, 64, good, good, 1e-6,

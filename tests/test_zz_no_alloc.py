@@ -50,6 +50,9 @@ def test_noalloc_matches_workspace_gemm_twice(cv):
     # second call: another shape and B layout, accumulating into C
     for M, N, K in ((128, 256, 4096), (200, 520, 2048)):
         assert cv.canvas_gemm_workspace_size(M, N, K) <= cv.CANVAS_GEMM_NOALLOC_SCRATCH_BYTES
+    # more than the 256-byte alignment slack: the first shape does split K, so
+    # its partials really go through the static array
+    assert cv.canvas_gemm_workspace_size(128, 256, 4096) > 256
     _compare(cv, 128, 256, 4096, 0, 0, seed=1)
     _compare(cv, 200, 520, 2048, 1, 1, seed=2)
 
@@ -64,3 +67,17 @@ def test_noalloc_rejects_shapes_beyond_the_static_scratch(cv):
         cv.canvas_gemm_bf16_noalloc(A, B, 0, C, 0)
     assert e.value.status == cv.CANVAS_ERR_WORKSPACE
     assert "static scratch" in str(e.value)
+
+
+def test_noalloc_rejects_a_misaligned_output(cv):
+    # C offset by one float: 4-byte aligned, not 16; the call returns before
+    # anything is enqueued
+    M, N, K = 128, 256, 4096
+    A = torch.zeros(M, K, device="cuda", dtype=torch.bfloat16)
+    B = torch.zeros(N, K, device="cuda", dtype=torch.bfloat16)
+    Cbig = torch.zeros(M * N + 4, device="cuda")
+    C = Cbig[1:1 + M * N].view(M, N)
+    with pytest.raises(cv.CanvasError) as e:
+        cv.canvas_gemm_bf16_noalloc(A, B, 0, C, 0)
+    assert e.value.status == cv.CANVAS_ERR_ARG
+    assert "aligned" in str(e.value)
