@@ -10,10 +10,13 @@ trained weights are involved.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --workload loop --prefix P [--steps K] [--warmup W]
+    python bench.py --workload sliding [--steps K] [--warmup W]
 
 Prints ONE JSON line (rank 0).  ``--workload loop`` times instead the batched
 denoising loop (4 canvases x 256, 5 sliding + 1 global layers, vocab 262144,
-committed prefix P), one line per run.  Under torchrun every rank runs its own step on
+committed prefix P), one line per run; ``--workload sliding`` times one
+sliding-window layer call (batch 1, canvas 256, prefix 4096, 16/8 heads,
+head_dim 256, window 1024).  Under torchrun every rank runs its own step on
 its own GPU (canvases are independent: weak scaling, no data-path
 collective); times are the max over ranks.  ``--impl reference`` times the
 fp64 CPU oracle (the reference arm of this tier) on bounded samples.
@@ -309,9 +312,9 @@ def run_ours(args, rank, world, local_rank):
     status = cv.canvas_device_status()
     assert status == cv.CANVAS_OK, cv.canvas_last_error()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    kern_ms = {names[kid]: statistics.mean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+    kern_ms = {names[kid]: statistics.median(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
                for j, kid in enumerate(ids)}
-    ms = max_over_ranks([statistics.mean(step_ms)], dev)[0]
+    ms = max_over_ranks([statistics.median(step_ms)], dev)[0]
 
     # ---- end to end: host inputs (pinned) -> device, results -> host, every step
     x_h = torch.empty(st.x.shape, dtype=torch.bfloat16).pin_memory()
@@ -344,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
             oh.copy_(o, non_blocking=True)
         e2e_ev[k][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks([statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)], dev)[0]
+    e2e_ms = max_over_ranks([statistics.median(a.elapsed_time(b) for a, b in e2e_ev)], dev)[0]
     assert cv.canvas_device_status() == cv.CANVAS_OK
 
     if rank != 0:
@@ -398,6 +401,130 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(st.a_in, st.s_in)
     return line
+
+
+# --------------------------------------------------------------------------- one sliding-window layer
+SLIDING_WORKLOAD = ("sliding-window layer: canvas_attention B=1 C=256 prefix=4096 D=2816 Hq=16 Hkv=8 d=256 "
+                    "window 1024 (full RoPE theta 1e4, paged bf16 cache of final keys and values, page 64)")
+
+
+def run_sliding(args, rank, world, local_rank):
+    """canvas_attention on the sliding-window layer workload: the call's rate,
+    and the attention core (kernel + KV-split combine) against the bf16 peak."""
+    import torch
+    import torch.distributed as dist
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import canvas_denoising_step_03_b300 as cv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c = wl.SLIDING
+    a = wl.make_attention_inputs(c)
+
+    def d16(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, W_q, W_k, W_v = d16(a.x), d16(a.W_q), d16(a.W_k), d16(a.W_v)
+    gq, gk, freq = (torch.from_numpy(t).to(dev) for t in (a.gamma_q, a.gamma_k, a.freq))
+    table, npages = wl.page_layout(c)
+    bt = torch.from_numpy(table).to(dev)
+    kp = d16(wl.scatter_pages(a.cache_k, table, npages, c.page_tokens))
+    vp = d16(wl.scatter_pages(a.cache_v, table, npages, c.page_tokens))
+    kv = cv.make_kv_cache(kp, vp, bt, c.page_tokens)
+    prefix = torch.from_numpy(a.prefix_len).to(dev)
+    out = torch.empty((c.B, c.C, c.Hq * c.d), dtype=torch.bfloat16, device=dev)
+    ws = cv.workspace(cv.canvas_attention_workspace_size(cv.CANVAS_BF16, c.B, c.C, c.D, c.Hq, c.Hkv, c.d,
+                                                         c.max_prefix, cv.CANVAS_LAYER_SLIDING), dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(xin):
+        cv.canvas_attention(xin, W_q, W_k, W_v, c.Hq, c.Hkv, c.d, gq, gk, c.eps, freq, cv.CANVAS_LAYER_SLIDING, kv,
+                            prefix, c.max_prefix, c.window, 1.0, 0, out, None, ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call(x)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    ids = [cv.CANVAS_KERNEL_PREP, cv.CANVAS_KERNEL_ATTENTION]
+    names = {cv.CANVAS_KERNEL_PREP: "attention_prep", cv.CANVAS_KERNEL_ATTENTION: "attention_core"}
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ids]
+          for _ in range(args.steps)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for row in ev:  # materialise the event handles (a torch event exists once recorded)
+        for e0, e1 in row:
+            e0.record()
+            e1.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = cv.canvas_kernel_launches()
+    for k in range(args.steps):
+        flush.fill_(1.0)
+        for kid, (e0, e1) in zip(ids, ev[k]):
+            cv.canvas_profile_events(kid, e0, e1)
+        step_ev[k][0].record(stream)
+        call(x)
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    launches = cv.canvas_kernel_launches() - launches0
+    clk = clocks.stop()
+    for kid in ids:
+        cv.canvas_profile_events(kid, None, None)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    kern_ms = {names[kid]: statistics.median(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+               for j, kid in enumerate(ids)}
+    ms = max_over_ranks([statistics.median(e0.elapsed_time(e1) for e0, e1 in step_ev)], dev)[0]
+    # end to end: x from pinned host memory in, the layer output out, every step
+    x_h = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+    x_h.copy_(x.cpu())
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        call(x_d)
+        out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        if k >= args.warmup:
+            e2e.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks([statistics.median(e0.elapsed_time(e1) for e0, e1 in e2e)], dev)[0]
+    if rank != 0:
+        return None
+    hbm, bf16, peak_src = measured_peaks()
+    af = attn_flops(c)
+    tfl = af / (kern_ms["attention_core"] * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(world * 1000.0 / ms, 3), "unit": "sliding-layer canvas_attention calls/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded draws; random weights and caches; no dataset)",
+        "config": {"workload": SLIDING_WORKLOAD,
+                   "l2": "flushed between timed calls (252 MB write, outside the call's events)",
+                   "parallelism": f"replicas x{world}"},
+        "attention_tflops": round(tfl, 2),
+        "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+        "roofline": {"kernel": "attention_core", "bound": "tensor", "achieved": round(tfl, 2), "peak": bf16,
+                     "unit": "TFLOP/s", "frac": round(tfl / bf16, 4), "traffic": None,
+                     "algorithmic": f"{af:.4g} FLOP per launch (4*d per visible query-key pair per head)",
+                     "peak_source": f"{peak_src} (burst)"},
+        "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "sliding-layer canvas_attention calls/s",
+                "h2d_bytes_per_step": int(x_h.numel() * 2), "d2h_bytes_per_step": int(out_h.numel() * 2)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
 
 
 # --------------------------------------------------------------------------- the batched loop
@@ -456,8 +583,8 @@ def run_loop(args, rank, world, local_rank):
         attn_ms.append(sum(per))
         sm = {n: e for n, e in marks if n.startswith("sample")}
         samp_ms.append(sm["sample_begin"].elapsed_time(sm["sample_end"]))
-    ms_core, ms_step = max_over_ranks([statistics.mean(a + s_ for a, s_ in zip(attn_ms, samp_ms)),
-                                       statistics.mean(step_ms)], dev)
+    ms_core, ms_step = max_over_ranks([statistics.median(a + s_ for a, s_ in zip(attn_ms, samp_ms)),
+                                       statistics.median(step_ms)], dev)
     # end to end: the step's result (tokens, commit mask) read back to pinned
     # host memory inside every timed step
     tok_h = torch.empty(run.tokens.shape, dtype=run.tokens.dtype).pin_memory()
@@ -470,12 +597,12 @@ def run_loop(args, rank, world, local_rank):
         mask_h.copy_(run.mask, non_blocking=True)
         e2e.append((t0, new_ev()))
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks([statistics.mean(a.elapsed_time(b) for a, b in e2e)], dev)[0]
+    e2e_ms = max_over_ranks([statistics.median(a.elapsed_time(b) for a, b in e2e)], dev)[0]
     if rank != 0:
         return None
     lcs = cfg.layer_cfgs()
     flops = [attn_flops(lc) for lc in lcs]
-    layer_mean = [statistics.mean(v) for v in layer_ms]
+    layer_mean = [statistics.median(v) for v in layer_ms]
     g = nl - 1  # the global layer
     hbm, bf16, peak_src = measured_peaks()
     g_tflops = flops[g] / (layer_mean[g] * 1e-3) / 1e12
@@ -493,7 +620,7 @@ def run_loop(args, rank, world, local_rank):
         "loop_ms_per_step": round(ms_step, 4),
         "attention_ms_per_layer": [round(v, 4) for v in layer_mean],
         "attention_tflops_per_layer": [round(f / (m * 1e-3) / 1e12, 1) for f, m in zip(flops, layer_mean)],
-        "sampler_ms": round(statistics.mean(samp_ms), 4),
+        "sampler_ms": round(statistics.median(samp_ms), 4),
         "roofline": {"kernel": "global-layer canvas_attention call (projections, key preparation, attention)",
                      "bound": "tensor", "achieved": round(g_tflops, 2), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(g_tflops / bf16, 4), "traffic": None,
@@ -625,7 +752,7 @@ def run_reference(args, rank, world):
         clock.run(clock.pieces[k % npieces], k)
         if k >= args.warmup:
             times.append(clock.estimate())
-    ms = statistics.mean(times) * 1000.0
+    ms = statistics.median(times) * 1000.0
     v = round(1000.0 / ms, 6)
     cores = blas_threads()
     desc = clock.describe()
@@ -644,7 +771,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="step", choices=["step", "loop"])
+    ap.add_argument("--workload", default="step", choices=["step", "loop", "sliding"])
     ap.add_argument("--prefix", type=int, default=1024, help="committed prefix of the loop workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
@@ -659,6 +786,8 @@ def main():
         line = run_reference(args, rank, world)
     elif args.workload == "loop":
         line = run_loop(args, rank, world, local_rank)
+    elif args.workload == "sliding":
+        line = run_sliding(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0 and line is not None:

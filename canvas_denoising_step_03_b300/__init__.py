@@ -143,7 +143,11 @@ def canvas_last_error() -> str:
 
 
 def canvas_profile_events(kernel_id: int, start=None, stop=None):
-    """Register torch.cuda.Event objects (or None) as timing hooks of a kernel."""
+    """Register torch.cuda.Event objects (or None) as timing hooks of a kernel.
+    A torch event has a CUDA handle only once it has been recorded."""
+    for e in (start, stop):
+        if e is not None and not e.cuda_event:
+            raise ValueError("canvas_profile_events: record the event once before registering it")
     hs = None if start is None else ctypes.c_void_p(start.cuda_event)
     he = None if stop is None else ctypes.c_void_p(stop.cuda_event)
     _check(lib.canvas_profile_events(int(kernel_id), hs, he))

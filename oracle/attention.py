@@ -144,18 +144,20 @@ def visible_prefix(P: int, i: int, window: int, layer: str) -> range:
     return range(max(0, P + i - window), P)
 
 
-def _row_slack(q, dq, keys, dkeys, vals, dvals, p, o, scale):
+def _row_slack(q, dq, abs_keys_hi, abs_dkeys, vals, abs_dvals, p, o, scale):
     """Bound on |o' - o| for one query row under every combination of flips.
 
-    q, dq [d]; keys, dkeys, vals, dvals [n, d]; p [n] softmax weights; o [d].
+    q, dq [d]; for the row's n visible keys: abs_keys_hi = |k_j| + |dk_j|,
+    abs_dkeys = |dk_j|, vals = v_j, abs_dvals = |dv_j| (all [n, d]); p [n]
+    softmax weights; o [d].
     Logit move bound D_j = scale * (|dq| . (|k_j| + |dk_j|) + |q| . |dk_j|).
     """
     aq, adq = np.abs(q), np.abs(dq)
-    D = abs(scale) * ((np.abs(keys) + np.abs(dkeys)) @ adq + np.abs(dkeys) @ aq)
+    D = abs(scale) * (abs_keys_hi @ adq + abs_dkeys @ aq)
     ed = np.exp(D)
     zmax = float(p @ ed)
     w = p * (zmax * ed - 1.0)
-    return w @ np.abs(vals - o) + (p * zmax * ed) @ np.abs(dvals)
+    return w @ np.abs(vals - o) + (p * zmax * ed) @ abs_dvals
 
 
 def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma_k,
@@ -206,9 +208,13 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
 
     for b in range(B):
         P = int(prefix_len[b])
+        if wanted is not None and not any(w[0] == b for w in wanted):
+            continue
         # 3-4: queries of this sequence, [Hq, C, d]
         q, dq = _store(rotate(rms(q_raw[b], gamma_q, eps), freq, P), storage, sl_eps)
         for hk in range(Hkv):
+            if wanted is not None and not any(w[0] == b and w[1] // G == hk for w in wanted):
+                continue
             # the key / value rows of this KV head: prefix then canvas
             if layer == "sliding":
                 kp = np.asarray(cache_k[b, hk, :P], np.float64)
@@ -241,14 +247,27 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     dvv = np.concatenate([np.zeros_like(rp), np.abs(drc) * (s_row * 1.01 if v_unit_rms else 1.0)])
                     dkp, dkc = dkk[:P], dkk[P:]
                     dvp, dvc = dvv[:P], dvv[P:]
+            # the keys of this head in position order, from the first prefix
+            # position any canvas row sees (row 0's) to the end of the canvas:
+            # a canvas row sees a range of prefix positions that ends at P,
+            # followed by the whole canvas -- rows vis.start - lo.. of these
+            lo = visible_prefix(P, 0, window, layer).start
+            keys_all = np.concatenate([kp[lo:], kc], axis=0)
+            vals_all = np.concatenate([vp[lo:], vc], axis=0)
+            if want_slack:
+                abs_dk_all = np.abs(np.concatenate([dkp[lo:], dkc], axis=0))
+                abs_k_hi_all = np.abs(keys_all) + abs_dk_all
+                abs_dv_all = np.abs(np.concatenate([dvp[lo:], dvc], axis=0))
             for g in range(G):
                 h = hk * G + g
                 for i in range(C):
                     if wanted is not None and (b, h, i) not in wanted:
                         continue
                     vis = visible_prefix(P, i, window, layer)
-                    keys = np.concatenate([kp[vis.start:vis.stop], kc], axis=0)
-                    vals = np.concatenate([vp[vis.start:vis.stop], vc], axis=0)
+                    assert vis.stop == P and vis.start >= lo
+                    j0 = vis.start - lo
+                    keys = keys_all[j0:]
+                    vals = vals_all[j0:]
                     s = scale * (keys @ q[h, i])
                     m = np.max(s)
                     e = np.exp(s - m)
@@ -257,9 +276,8 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     out[b, i, h * d:(h + 1) * d] = o
                     lse[b, i, h] = m + np.log(Z)
                     if want_slack:
-                        dkeys = np.concatenate([dkp[vis.start:vis.stop], dkc], axis=0)
-                        dvals = np.concatenate([dvp[vis.start:vis.stop], dvc], axis=0)
-                        slack[b, i, h * d:(h + 1) * d] = _row_slack(q[h, i], dq[h, i], keys, dkeys, vals, dvals,
+                        slack[b, i, h * d:(h + 1) * d] = _row_slack(q[h, i], dq[h, i], abs_k_hi_all[j0:],
+                                                                    abs_dk_all[j0:], vals, abs_dv_all[j0:],
                                                                     e / Z, o, scale)
     if want_slack:
         return out, lse, slack

@@ -45,17 +45,19 @@ def loop_step(layers, E: np.ndarray, tokens: np.ndarray, soft_prev: Optional[np.
     W_v, W_o, gamma_q, gamma_k, freq, eps, Hq, Hkv, d, layer, window,
     cache_k, cache_v [dense by position], prefix).  Returns a dict with the
     residual stream before every layer and after the last (``xs``, fp64
-    [rows, D]), the per-layer attention outputs (bf16-rounded, [B, C, Hq*d])
-    and, with ``slack_eps``, their rounding slack; the bf16 logits (all rows,
-    or only ``sample_rows`` -- NaN elsewhere) and the sampler outputs of those
-    rows (soft_emb for them)."""
+    [rows, D]), the per-layer attention outputs (``attn``: bf16-rounded as
+    stored, ``attn_exact``: before that rounding; [B, C, Hq*d]) and, with
+    ``slack_eps``, their rounding slack; the bf16 logits (all rows, or only
+    ``sample_rows`` -- NaN elsewhere) and the sampler outputs of those rows
+    (soft_emb for them)."""
     rows = B * C
     D = E.shape[1]
+    sel = np.arange(rows) if sample_rows is None else np.asarray(sorted(set(sample_rows)), np.int64)
     v = E[np.asarray(tokens, np.int64)]
     if soft_prev is not None:
         v = v + soft_prev
     x = v.copy()
-    xs, outs, slacks = [x.copy()], [], []
+    xs, outs, exact, slacks = [x.copy()], [], [], []
     for L in layers:
         xb = bf16_round(x).reshape(B, C, D)
         res = canvas_attention(xb, L["W_q"], L["W_k"], L["W_v"], L["Hq"], L["Hkv"], L["d"], L["gamma_q"],
@@ -64,12 +66,12 @@ def loop_step(layers, E: np.ndarray, tokens: np.ndarray, soft_prev: Optional[np.
         out = res[0]
         if slack_eps is not None:
             slacks.append(res[2])
+        exact.append(out)
         ob = bf16_round(out).reshape(rows, -1)
         outs.append(ob.reshape(B, C, -1))
         x = x + ob @ L["W_o"].T
         xs.append(x.copy())
     xb = bf16_round(x)
-    sel = np.arange(rows) if sample_rows is None else np.asarray(sorted(set(sample_rows)), np.int64)
     logits = np.full((rows, E.shape[0]), np.nan)
     logits[sel] = bf16_round(xb[sel] @ E.T)
     # the sampler of the selected rows (each keeps its global row index for
@@ -77,7 +79,7 @@ def loop_step(layers, E: np.ndarray, tokens: np.ndarray, soft_prev: Optional[np.
     fr = None if frozen is None else np.asarray(frozen)[sel]
     ft = None if frozen_tokens is None else np.asarray(frozen_tokens)[sel]
     res = _sample_rows(logits[sel], E, bound, seed, step, C, fr, ft, sel)
-    return dict(attn=outs, slack=slacks, logits=logits, xs=xs, x=xb, rows=sel, **res)
+    return dict(attn=outs, attn_exact=exact, slack=slacks, logits=logits, xs=xs, x=xb, rows=sel, **res)
 
 
 def _sample_rows(logits, E, bound, seed, step, C, frozen, frozen_tokens, rows):

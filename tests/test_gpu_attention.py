@@ -1,39 +1,31 @@
 """canvas_attention through the C ABI against the fp64 oracle.
 
 Tolerances: bf16 calls -- max |err| <= 2e-2 and relative Frobenius error
-<= 5e-3 (the bar set for the attention output in bf16); fp32 calls -- 1e-4 /
-1e-5 (fp32 arithmetic against fp64).
+<= 5e-3 (the bar set for the attention output in bf16), with the two
+refinements of canvas_harness.judge_attention (half a bf16 spacing for
+|value| >= 8; the oracle's rounding slack downstream of rounding ties, on at
+most MAX_FRAC_OVER of the elements); each case records plain max |err|, the
+number of elements above 2e-2, the number that needed slack, and the distance
+to the oracle without any bf16 rounding.  fp32 calls -- 1e-4 / 1e-5 (fp32
+arithmetic against fp64).
 
 bf16 storage decisions.  The path stores q, the canvas keys / values and the
 global keys in bf16; the oracle rounds the same tensors at the same points.
 Where an exact value lies within the path's fp32 arithmetic error of a bf16
-rounding midpoint both neighbours are correct stored values, and the sharp
-softmax of these workloads can turn such a flip into an output change above
-2e-2.  For every output element the oracle bounds that change over all
-combinations of such flips (``slack``); an element passes when
-|err| <= 2e-2 + slack.  Elements with no ambiguous decision upstream have
-slack 0 and face the plain 2e-2 bar; the relative Frobenius bar has no slack.
-The ambiguity window SLACK_EPS covers the path's measured fp32 error before
-rounding (projection + norm + rotation).  The output itself is stored in
-bf16, so the 2e-2 bar is floored at one bf16 spacing of the value (above
-|o| = 4 the spacing exceeds 2e-2).
+rounding midpoint both neighbours are correct stored values (a rounding tie),
+and the sharp softmax of these workloads can turn such a flip into an output
+change above 2e-2.  For every output element the oracle bounds that change
+over all combinations of such flips (``slack``).
 """
 import numpy as np
 import pytest
 import torch
 
 import canvas_workloads as wl
-from canvas_harness import AttnCase, attn_errors, oracle_attention
+from canvas_harness import SLACK_EPS, AttnCase, attn_errors, judge_attention, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
-BF16_MAX, BF16_FRO = 2e-2, 5e-3
-# ambiguity window relative to |x| + |pair partner| + row rms: twice the largest
-# fp32 projection error measured on the workloads (4.1e-6 of the row rms)
-SLACK_EPS = 2.0 ** -17
-# at most this fraction of the elements may need slack at all (measured: 1.7e-4 on
-# the global layer of the loop workload, 1.8e-5 on the sliding workload)
-MAX_FRAC_OVER = 1e-3
 FP32_MAX, FP32_FRO = 1e-4, 1e-5
 
 
@@ -45,13 +37,6 @@ def cv():
     return cv
 
 
-def bf16_spacing(a):
-    """Distance between consecutive bf16 values around |a| (8 significant bits)."""
-    a = np.abs(np.asarray(a, np.float64))
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    return np.ldexp(1.0, (e - 7).astype(int))
-
-
 def small(**kw):
     base = dict(name="small", B=2, C=80, prefix=(300, 130), D=256, Hq=4, Hkv=2, d=128, layer="sliding",
                 window=96, theta=1e4, rotary_fraction=1.0, dtype="bf16", seed=21, page_tokens=64)
@@ -59,23 +44,16 @@ def small(**kw):
     return wl.AttnConfig(**base)
 
 
-def check(cv, cfg, rows=None, v_unit_rms=False, page_seed=1234):
+def check(cv, cfg, rows=None, v_unit_rms=False, page_seed=1234, name=None):
     inp = wl.make_attention_inputs(cfg)
     case = AttnCase(inp, page_seed=page_seed).run(v_unit_rms=int(v_unit_rms))
     assert case.status() == cv.CANVAS_OK, cv.canvas_last_error()
     got = case.out_f64()
     if cfg.dtype == "bf16":
         want, want_lse, slack = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms, slack_eps=SLACK_EPS)
-        mx, rf = attn_errors(got, want)
-        m = np.isfinite(want)
-        err = np.abs(got - want)[m]
-        bar = np.maximum(BF16_MAX, bf16_spacing(want[m]))
-        over = err > bar
-        print(f"{cfg.name}: max|err| {mx:.4g}, rel-Fro {rf:.3g}, {int(over.sum())} of {err.size} elements above "
-              f"the bar (largest slack used {float(np.max(slack[m][over], initial=0.0)):.3g})")
-        assert rf <= BF16_FRO, rf
-        assert np.all(err <= bar + slack[m]), float(np.max(err - bar - slack[m]))
-        assert over.mean() <= MAX_FRAC_OVER, over.mean()
+        want64, _ = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms, storage="fp64")
+        rec = judge_attention(name or cfg.name, got, want, slack, want64)
+        mx, rf = rec["max_abs_err"], rec["rel_fro"]
     else:
         want, want_lse = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms)
         mx, rf = attn_errors(got, want)

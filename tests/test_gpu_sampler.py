@@ -17,6 +17,14 @@ pytestmark = pytest.mark.gpu
 TIE = 1e-6
 
 
+def onum_spacing(a):
+    """Distance between consecutive bf16 values around |a| (8 significant bits;
+    normal range)."""
+    a = np.abs(np.asarray(a, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.ldexp(1.0, (e - 7).astype(int))
+
+
 @pytest.fixture(scope="module")
 def cv():
     import __graft_entry__
@@ -101,6 +109,22 @@ def test_peaked_and_flat_rows(cv, dtype):
                               s.cfg.step, canvas_len=s.cfg.C, probs_storage=st)
     assert 0 < ref["commit_mask"].sum() < s.cfg.rows
     compare(cv, s, run, ref)
+    got = run.probs.float().cpu().numpy().astype(np.float64)
+    if dtype == "bf16":
+        # each stored bf16 probability is a correct rounding of a value within
+        # the path's fp32 error (2^-17 relative: the exponential, its scaled
+        # argument and the 1/Z product) of the exact probability
+        exact = osamp.canvas_sample(wl.as_f64(s.logits, dtype), None, s.cfg.bound, s.cfg.seed, s.cfg.step,
+                                    canvas_len=s.cfg.C)["probs"]
+        bar = 0.5 * onum_spacing(exact) + 2.0 ** -17 * exact
+        err = np.abs(got - exact)
+        assert np.all(err <= bar), float(np.max(err - bar))
+        # and equal to the oracle's own stored value away from rounding ties
+        mid = np.abs(exact - ref["probs"]) < 0.5 * onum_spacing(exact) - 2.0 ** -17 * exact
+        assert np.array_equal(got[mid], ref["probs"][mid])
+        print(f"bf16 probabilities: {int((~mid).sum())} of {mid.size} within the fp32 error of a rounding tie")
+    else:
+        np.testing.assert_allclose(got, ref["probs"], rtol=1e-5, atol=1e-12)
 
 
 def test_temperature_prefix_mode_and_frozen(cv):

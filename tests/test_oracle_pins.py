@@ -471,7 +471,7 @@ def test_row_slack_bounds_brute_force_flips(which):
     s = keys @ q
     p = np.exp(s - s.max())
     p /= p.sum()
-    bound = oatt._row_slack(q, dq, keys, dk, vals, dv, p, base, 1.0)
+    bound = oatt._row_slack(q, dq, np.abs(keys) + np.abs(dk), np.abs(dk), vals, np.abs(dv), p, base, 1.0)
     worst = np.zeros(d)
     import itertools
     for mask in itertools.product([0, 1], repeat=len(flips)):
