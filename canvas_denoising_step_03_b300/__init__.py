@@ -39,6 +39,8 @@ EXPORTED = [
     "canvas_gemm_workspace_size", "canvas_gemm_bf16", "canvas_last_error", "canvas_device_status",
     "canvas_version", "canvas_profile_events", "canvas_kernel_launches", "canvas_gemm_bf16_noalloc",
     "canvas_embed_input", "canvas_cast_bf16", "canvas_gemm_bf16_to_bf16", "canvas_selftest_wait_timeout",
+    "canvas_attention_encode", "canvas_kv_append_workspace_size", "canvas_kv_append", "canvas_count_committed",
+    "canvas_temperature_at", "canvas_gelu_bf16",
 ]
 
 # size of the static scratch behind canvas_gemm_bf16_noalloc (include/canvas.h)
@@ -73,6 +75,19 @@ def _load(path: str = LIB_PATH):
     lib.canvas_attention.argtypes = [P, I, I, I, I, P, P, P, I, I, I, P, P, F, P, I,
                                      ctypes.POINTER(canvas_kv_cache), P, I, I, F, I, P, P, P, Z, P]
     lib.canvas_attention.restype = I
+    lib.canvas_attention_encode.argtypes = lib.canvas_attention.argtypes
+    lib.canvas_attention_encode.restype = I
+    lib.canvas_kv_append_workspace_size.argtypes = [I] * 7
+    lib.canvas_kv_append_workspace_size.restype = Z
+    lib.canvas_kv_append.argtypes = [P, I, I, I, I, P, P, I, I, P, F, P, I, ctypes.POINTER(canvas_kv_cache), P, I,
+                                     P, Z, P]
+    lib.canvas_kv_append.restype = I
+    lib.canvas_gelu_bf16.argtypes = [P, P, Z, P]
+    lib.canvas_gelu_bf16.restype = I
+    lib.canvas_count_committed.argtypes = [P, I, I, P, P]
+    lib.canvas_count_committed.restype = I
+    lib.canvas_temperature_at.argtypes = [I, I, F, F]
+    lib.canvas_temperature_at.restype = F
     lib.canvas_sample_workspace_size.argtypes = [I, I, I, I]
     lib.canvas_sample_workspace_size.restype = Z
     lib.canvas_sample.argtypes = [P, I, I, I, P, I, F, U64, U32, F, I, I, P, P, P, P, P, P, P, P, I, P, P, Z, P]
@@ -190,6 +205,32 @@ def canvas_attention(x, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, 
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def canvas_attention_encode(x, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, layer_type,
+                            kv: canvas_kv_cache, prefix_len, max_prefix, window, scale, v_unit_rms, out, lse,
+                            workspace, stream=None):
+    """canvas_attention in encode mode (causal inside the block); same arguments."""
+    B, C, D = x.shape
+    _check(lib.canvas_attention_encode(_ptr(x), _dtype_code(x), B, C, D, _ptr(W_q), _ptr(W_k), _ptr(W_v), Hq, Hkv,
+                                       d, _ptr(gamma_q), _ptr(gamma_k), float(eps), _ptr(freq), int(layer_type),
+                                       ctypes.byref(kv), _ptr(prefix_len), int(max_prefix), int(window),
+                                       float(scale), int(v_unit_rms), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def canvas_kv_append_workspace_size(dtype: int, B, C, D, Hkv, d, layer_type) -> int:
+    return lib.canvas_kv_append_workspace_size(dtype, B, C, D, Hkv, d, layer_type)
+
+
+def canvas_kv_append(x, W_k, W_v, Hkv, d, gamma_k, eps, freq, layer_type, kv: canvas_kv_cache, prefix_len,
+                     max_prefix, workspace, stream=None):
+    """Write a committed block's cache rows; advances prefix_len by C."""
+    B, C, D = x.shape
+    _check(lib.canvas_kv_append(_ptr(x), _dtype_code(x), B, C, D, _ptr(W_k), _ptr(W_v), Hkv, d, _ptr(gamma_k),
+                                float(eps), _ptr(freq), int(layer_type), ctypes.byref(kv), _ptr(prefix_len),
+                                int(max_prefix), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
+
+
 def canvas_sample(logits, E, entropy_bound, seed, step, temperature, commit_mode, canvas_len, frozen,
                   frozen_tokens, tokens, commit_mask, entropy, confidence, argmax, probs_out, probs_dtype,
                   soft_emb, workspace, stream=None):
@@ -201,6 +242,22 @@ def canvas_sample(logits, E, entropy_bound, seed, step, temperature, commit_mode
                              _ptr(entropy), _ptr(confidence), _ptr(argmax), _ptr(probs_out), int(probs_dtype),
                              _ptr(soft_emb), _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def canvas_gelu_bf16(inp, out, stream=None):
+    """out = bf16(gelu(inp)) (tanh form), inp fp32."""
+    _check(lib.canvas_gelu_bf16(_ptr(inp), _ptr(out), inp.numel(), _stream(stream)))
+
+
+def canvas_count_committed(commit_mask, canvas_len, counts, stream=None):
+    """counts[c] = committed positions of canvas c (commit_mask [rows] uint8)."""
+    _check(lib.canvas_count_committed(_ptr(commit_mask), commit_mask.numel(), int(canvas_len), _ptr(counts),
+                                      _stream(stream)))
+
+
+def canvas_temperature_at(step: int, steps: int, t_max: float, t_min: float) -> float:
+    """Sampler temperature of a step on the linear t_max -> t_min schedule."""
+    return float(lib.canvas_temperature_at(int(step), int(steps), float(t_max), float(t_min)))
 
 
 def canvas_gemm_bf16(A, B, b_layout, C, accumulate, workspace, stream=None):

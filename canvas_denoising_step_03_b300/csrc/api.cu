@@ -190,7 +190,7 @@ size_t gemm_ws_bytes(const GemmPlan& p) { return align_up(p.partial_bytes); }
 // split partials.
 canvas_status run_gemm_group(const void* A, const void* const* B, void* const* C, const int* N, int nprob,
                              int b_mn_major, int M, int K, int accumulate, int out_bf16, void* ws,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float** partials_out = nullptr, int* splits_out = nullptr) {
   if (nprob < 1 || nprob > kGemmMaxProblems) return fail(CANVAS_ERR_ARG, "GEMM: 1 to 3 problems per launch");
   const GemmPlan p = plan_gemm_group(M, N, nprob, K);
   GemmTcMaps maps;
@@ -236,7 +236,13 @@ canvas_status run_gemm_group(const void* A, const void* const* B, void* const* C
   g.two_acc = p.two_acc;
   g.m_tiles = p.m_tiles;
   g.nprob = nprob;
-  CANVAS_CUDA(launch_gemm_tc(maps, g, stream));
+  // partials_out: the caller sums a split product's partials itself
+  const bool reduce = partials_out == nullptr;
+  CANVAS_CUDA(launch_gemm_tc(maps, g, stream, reduce));
+  if (!reduce) {
+    for (int i = 0; i < nprob; ++i) partials_out[i] = p.splits > 1 ? g.partials[i] : static_cast<float*>(C[i]);
+    *splits_out = p.splits;
+  }
   return CANVAS_OK;
 }
 
@@ -368,6 +374,34 @@ canvas_status canvas_device_status(canvas_stream_t stream) {
   return CANVAS_OK;
 }
 
+canvas_status canvas_gelu_bf16(const float* in, void* out, size_t n, canvas_stream_t stream) {
+  if (!in || !out) return fail(CANVAS_ERR_ARG, "canvas_gelu_bf16: null pointer");
+  if (n % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gelu_bf16: n must be a multiple of 8");
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_gelu_bf16: pointers must be 16-byte aligned");
+  if (n == 0) return CANVAS_OK;
+  CANVAS_CUDA(launch_gelu_bf16(in, out, (long long)n, reinterpret_cast<cudaStream_t>(stream)));
+  return CANVAS_OK;
+}
+
+canvas_status canvas_count_committed(const uint8_t* commit_mask, int rows, int canvas_len, int32_t* counts,
+                                     canvas_stream_t stream) {
+  if (!commit_mask || !counts) return fail(CANVAS_ERR_ARG, "canvas_count_committed: null pointer");
+  if (rows < 1 || canvas_len < 1 || rows % canvas_len != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_count_committed: rows must be a multiple of canvas_len");
+  CANVAS_CUDA(launch_count_committed(commit_mask, rows / canvas_len, canvas_len, counts,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+  return CANVAS_OK;
+}
+
+float canvas_temperature_at(int step, int steps, float t_max, float t_min) {
+  // linear from t_max at step 0 to t_min at step steps - 1 (one step: t_max)
+  if (steps <= 1 || step <= 0) return t_max;
+  if (step >= steps - 1) return t_min;
+  const double f = double(step) / double(steps - 1);
+  return float(double(t_max) + (double(t_min) - double(t_max)) * f);
+}
+
 canvas_status canvas_selftest_wait_timeout(canvas_stream_t stream) {
   CANVAS_CUDA(launch_wait_timeout_selftest(reinterpret_cast<cudaStream_t>(stream)));
   return CANVAS_OK;
@@ -481,11 +515,14 @@ size_t canvas_attention_workspace_size(int dtype, int B, int C, int D, int Hq, i
   return attn_layout(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type, 0).total;  // window 0: the largest plan
 }
 
-canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, const void* W_q, const void* W_k,
-                               const void* W_v, int Hq, int Hkv, int d, const float* gamma_q, const float* gamma_k,
-                               float eps, const float* freq, int layer_type, const canvas_kv_cache* kv,
-                               const int32_t* prefix_len, int max_prefix, int window, float scale, int v_unit_rms,
-                               void* out, float* lse, void* workspace, size_t ws_bytes, canvas_stream_t stream_) {
+// canvas_attention (decode mode, causal = 0) and canvas_attention_encode
+// (encode mode, causal = 1)
+static canvas_status attention_impl(const void* x, int dtype, int B, int C, int D, const void* W_q, const void* W_k,
+                             const void* W_v, int Hq, int Hkv, int d, const float* gamma_q, const float* gamma_k,
+                             float eps, const float* freq, int layer_type, const canvas_kv_cache* kv,
+                             const int32_t* prefix_len, int max_prefix, int window, float scale, int v_unit_rms,
+                             void* out, float* lse, void* workspace, size_t ws_bytes, canvas_stream_t stream_,
+                             int causal) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!attn_shape_ok(dtype, B, C, D, Hq, Hkv, d, max_prefix, layer_type))
     return fail(CANVAS_ERR_ARG, "canvas_attention: invalid shape or dtype");
@@ -534,13 +571,20 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
 
   // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
   mark_start(CANVAS_KERNEL_PREP, stream);
+  int proj_splits = 1;
   if (bf16) {
     // one launch for the two or three products (they share x)
     const void* Ws[3] = {W_q, W_k, W_v};
     void* outs[3] = {proj_q, proj_k, proj_v};
     const int Ns[3] = {Hq * d, Hkv * d, Hkv * d};
-    const canvas_status st = run_gemm_group(x, Ws, outs, Ns, global ? 2 : 3, 0, M, D, 0, 0, gws, stream);
+    // a split product stays in its partials: the prologue sums them
+    float* parts[3] = {nullptr, nullptr, nullptr};
+    const canvas_status st =
+        run_gemm_group(x, Ws, outs, Ns, global ? 2 : 3, 0, M, D, 0, 0, gws, stream, parts, &proj_splits);
     if (st != CANVAS_OK) return st;
+    proj_q = parts[0];
+    proj_k = parts[1];
+    if (!global) proj_v = parts[2];
   } else {
     CANVAS_CUDA(launch_gemm_simt(x, W_q, 0, false, proj_q, M, Hq * d, D, 0, stream));
     CANVAS_CUDA(launch_gemm_simt(x, W_k, 0, false, proj_k, M, Hkv * d, D, 0, stream));
@@ -551,6 +595,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
   p.proj_q = proj_q;
   p.proj_k = proj_k;
   p.proj_v = global ? nullptr : proj_v;
+  p.splits = proj_splits;
   p.gamma_q = gamma_q;
   p.gamma_k = gamma_k;
   p.freq = freq;
@@ -652,6 +697,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     // key block, so no S is formed twice); 2-SM MMAs do not pay at head_dim
     // 256 (166 -> 178 us), where one SM per tile stays
     t.pair = quad ? 2 : 0;
+    t.causal = causal;
     t.Qp = static_cast<const __nv_bfloat16*>(Qp);
     t.block_table = kv->block_table;
     t.max_pages = kv->max_pages_per_seq;
@@ -693,6 +739,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     a.Tpad = pl.Tpad;
     a.global = global ? 1 : 0;
     a.v_unit_rms = v_unit_rms ? 1 : 0;
+    a.causal = causal;
     a.scale = scale;
     a.out = out;
     a.lse = lse;
@@ -700,6 +747,109 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
     CANVAS_CUDA(launch_attention_simt(a, bf16, stream));
     mark_stop(CANVAS_KERNEL_ATTENTION, stream);
   }
+  return CANVAS_OK;
+}
+
+canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, const void* W_q, const void* W_k,
+                               const void* W_v, int Hq, int Hkv, int d, const float* gamma_q, const float* gamma_k,
+                               float eps, const float* freq, int layer_type, const canvas_kv_cache* kv,
+                               const int32_t* prefix_len, int max_prefix, int window, float scale, int v_unit_rms,
+                               void* out, float* lse, void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  return attention_impl(x, dtype, B, C, D, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, layer_type, kv,
+                        prefix_len, max_prefix, window, scale, v_unit_rms, out, lse, workspace, ws_bytes, stream, 0);
+}
+
+canvas_status canvas_attention_encode(const void* x, int dtype, int B, int C, int D, const void* W_q,
+                                      const void* W_k, const void* W_v, int Hq, int Hkv, int d,
+                                      const float* gamma_q, const float* gamma_k, float eps, const float* freq,
+                                      int layer_type, const canvas_kv_cache* kv, const int32_t* prefix_len,
+                                      int max_prefix, int window, float scale, int v_unit_rms, void* out, float* lse,
+                                      void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  return attention_impl(x, dtype, B, C, D, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, layer_type, kv,
+                        prefix_len, max_prefix, window, scale, v_unit_rms, out, lse, workspace, ws_bytes, stream, 1);
+}
+
+// ------------------------------------------------------------------ block commit
+static size_t kv_append_ws(int dtype, int B, int C, int D, int Hkv, int d, int layer_type, size_t* gemm_ws) {
+  const size_t M = size_t(B) * C;
+  const bool global = layer_type == CANVAS_LAYER_GLOBAL;
+  const size_t proj = M * Hkv * d * 4;
+  size_t g = 0;
+  if (dtype == CANVAS_BF16) {
+    const int Ns[2] = {Hkv * d, Hkv * d};
+    g = gemm_ws_bytes(plan_gemm_group(int(M), Ns, global ? 1 : 2, D));
+  }
+  if (gemm_ws) *gemm_ws = g;
+  return align_up(proj) + (global ? 0 : align_up(proj)) + align_up(g) + kAlign;
+}
+
+size_t canvas_kv_append_workspace_size(int dtype, int B, int C, int D, int Hkv, int d, int layer_type) {
+  if ((dtype != CANVAS_BF16 && dtype != CANVAS_FP32) || B < 1 || C < 1 || D < 1 || Hkv < 1 || d < 2) return 0;
+  if (layer_type != CANVAS_LAYER_SLIDING && layer_type != CANVAS_LAYER_GLOBAL) return 0;
+  return kv_append_ws(dtype, B, C, D, Hkv, d, layer_type, nullptr);
+}
+
+canvas_status canvas_kv_append(const void* x, int dtype, int B, int C, int D, const void* W_k, const void* W_v,
+                               int Hkv, int d, const float* gamma_k, float eps, const float* freq, int layer_type,
+                               const canvas_kv_cache* kv, int32_t* prefix_len, int max_prefix, void* workspace,
+                               size_t ws_bytes, canvas_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t need = canvas_kv_append_workspace_size(dtype, B, C, D, Hkv, d, layer_type);
+  if (need == 0) return fail(CANVAS_ERR_ARG, "canvas_kv_append: invalid shape, dtype or layer type");
+  const bool global = layer_type == CANVAS_LAYER_GLOBAL;
+  const bool bf16 = dtype == CANVAS_BF16;
+  if (!x || !W_k || !gamma_k || !freq || !kv || !prefix_len || !kv->k_pool || !kv->block_table)
+    return fail(CANVAS_ERR_ARG, "canvas_kv_append: null pointer");
+  if (global && (W_v != nullptr || kv->v_pool != nullptr))
+    return fail(CANVAS_ERR_ARG, "canvas_kv_append: global layers keep one raw shared pool (W_v and v_pool NULL)");
+  if (!global && (W_v == nullptr || kv->v_pool == nullptr))
+    return fail(CANVAS_ERR_ARG, "canvas_kv_append: sliding layers need W_v and v_pool");
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0) return fail(CANVAS_ERR_ARG, "canvas_kv_append: x must be 16-byte aligned");
+  if (kv->page_tokens < 1 || kv->num_pages < 1 || kv->max_pages_per_seq < 1 || max_prefix < C ||
+      (long long)kv->max_pages_per_seq * kv->page_tokens < max_prefix)
+    return fail(CANVAS_ERR_ARG, "canvas_kv_append: cache geometry cannot hold max_prefix tokens");
+  if (d % 64 != 0 || d > 512) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_kv_append: head_dim must be 64, 128, ..., 512");
+  if (bf16 && ((d & (d - 1)) != 0 || D % 8 != 0))
+    return fail(CANVAS_ERR_UNSUPPORTED, "canvas_kv_append: bf16 needs head_dim 64, 128, 256 or 512 and D a multiple of 8");
+  if (!ws_ok(workspace, ws_bytes, need))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_kv_append: workspace missing, small or misaligned (need %zu)", need);
+  size_t gws_bytes = 0;
+  kv_append_ws(dtype, B, C, D, Hkv, d, layer_type, &gws_bytes);
+  const size_t M = size_t(B) * C;
+  Carver cv(workspace);
+  float* proj_k = cv.take<float>(M * Hkv * d * 4);
+  float* proj_v = global ? nullptr : cv.take<float>(M * Hkv * d * 4);
+  void* gws = cv.take<char>(gws_bytes);
+  if (bf16) {
+    const void* Ws[2] = {W_k, W_v};
+    void* outs[2] = {proj_k, proj_v};
+    const int Ns[2] = {Hkv * d, Hkv * d};
+    const canvas_status st = run_gemm_group(x, Ws, outs, Ns, global ? 1 : 2, 0, int(M), D, 0, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+  } else {
+    CANVAS_CUDA(launch_gemm_simt(x, W_k, 0, false, proj_k, int(M), Hkv * d, D, 0, stream));
+    if (!global) CANVAS_CUDA(launch_gemm_simt(x, W_v, 0, false, proj_v, int(M), Hkv * d, D, 0, stream));
+  }
+  KvAppendArgs p;
+  p.proj_k = proj_k;
+  p.proj_v = proj_v;
+  p.gamma_k = gamma_k;
+  p.freq = freq;
+  p.prefix_len = prefix_len;
+  p.k_pool = const_cast<void*>(kv->k_pool);
+  p.v_pool = const_cast<void*>(kv->v_pool);
+  p.block_table = kv->block_table;
+  p.max_pages = kv->max_pages_per_seq;
+  p.page_tokens = kv->page_tokens;
+  p.num_pages = kv->num_pages;
+  p.B = B;
+  p.C = C;
+  p.Hkv = Hkv;
+  p.d = d;
+  p.max_prefix = max_prefix;
+  p.eps = eps;
+  p.global = global ? 1 : 0;
+  CANVAS_CUDA(launch_kv_append(p, bf16, stream));
   return CANVAS_OK;
 }
 
@@ -722,8 +872,8 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
   if ((frozen == nullptr) != (frozen_tokens == nullptr))
     return fail(CANVAS_ERR_ARG, "canvas_sample: frozen and frozen_tokens go together");
   if (!(temperature > 0.f)) return fail(CANVAS_ERR_ARG, "canvas_sample: temperature must be > 0");
-  if (commit_mode != 0 && commit_mode != 1) return fail(CANVAS_ERR_ARG, "canvas_sample: commit_mode");
-  if (canvas_len < 1 || (commit_mode == 1 && rows % canvas_len != 0))
+  if (commit_mode < 0 || commit_mode > 3) return fail(CANVAS_ERR_ARG, "canvas_sample: commit_mode");
+  if (canvas_len < 1 || ((commit_mode & 1) && rows % canvas_len != 0))
     return fail(CANVAS_ERR_ARG, "canvas_sample: canvas_len");
   if (probs_out && probs_dtype != CANVAS_BF16 && probs_dtype != CANVAS_FP32)
     return fail(CANVAS_ERR_ARG, "canvas_sample: probs_dtype");

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(1024) attention_simt_kernel(AttnArgs a) {
   if (P < 0 || P > a.max_prefix) return;  // reported by the key-prep kernel
   const int P64 = P & ~63;
   const int lo = (a.global || a.window <= 0) ? 0 : max(0, P + i - a.window);
-  const int n_keys = P + a.C - lo;
+  const int n_keys = (a.causal ? P + i + 1 : P + a.C) - lo;  // encode mode: canvas keys 0..i
   const size_t grp = (size_t)b * a.Hkv + hk;
 
   // this warp's query row

@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pos0 = sq.P64 + t0;
         hi_off = min(64, sq.T - t0);
       }
+      // encode mode: canvas keys up to the row's own position
+      if (a.causal && valid) hi_off = min(hi_off, sq.P + i + 1 - pos0);
       // visible offsets [lo_off, hi_off): position >= the row's window start
       // (lo_row <= P, so canvas keys pass) and, in the tail, before the padding
       const int lo_off = max(0, lo_row - pos0);
@@ -866,6 +868,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
         pos0 = sq.P64 + t0;
         hi_off = min(64, sq.T - t0);
       }
+      // encode mode: canvas keys up to the row's own position
+      if (a.causal && valid) hi_off = min(hi_off, sq.P + i + 1 - pos0);
       const int lo_off = max(0, lo_row - pos0);
       uint32_t sv[64];
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));

@@ -390,6 +390,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (the two-wide FMA / add of sm_100-class SMs: one
+// instruction for two lanes of arithmetic, each correctly rounded).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return (uint64_t(__float_as_uint(hi)) << 32) | uint64_t(__float_as_uint(lo));
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// The two bf16 values of a packed word as a pair of fp32 (exact).
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
+  return (uint64_t(w & 0xffff0000u) << 32) | uint64_t(w << 16);
+}
+
 // cos / sin of the RoPE angle pos * freq.  freq is split into turns,
 // g = freq / (2 pi) = g_hi + g_lo: the product of freq with 1 / (2 pi) held
 // as two fp32 parts (c_hi + c_lo, residual below 2^-50 relative), the rounding

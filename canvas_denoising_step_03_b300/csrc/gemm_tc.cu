@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(256) gemm_split_reduce_kernel(const float4* __
   }
 }
 
-cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStream_t stream) {
+cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStream_t stream, bool reduce) {
   static bool attr_set = false;  // per process; the attribute is per function
   const size_t smem = gemm_tc_smem_bytes();
   if (!attr_set) {
@@ -291,7 +291,7 @@ cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStre
   gemm_bf16_tc_kernel<<<grid, kThreads, smem, stream>>>(maps, g);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || g.splits == 1) return e;
+  if (e != cudaSuccess || g.splits == 1 || !reduce) return e;
   for (int p = 0; p < g.nprob; ++p) {
     const long long n4 = (long long)g.M * g.N[p] / 4;  // N % 8 == 0
     const int blocks = int(std::min<long long>((n4 + 255) / 256, 148LL * 8));

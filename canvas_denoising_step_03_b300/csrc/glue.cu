@@ -66,6 +66,40 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float4* __restrict
   }
 }
 
+// out = bf16(gelu(in)), GELU in its tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x +
+// 0.044715 x^3))) evaluated in fp32 (tanhf), rounded once: the activation of
+// the self-conditioning MLP.
+__global__ void __launch_bounds__(256) gelu_bf16_kernel(const float4* __restrict__ in, uint4* __restrict__ out,
+                                                        long long n8) {
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+  for (long long e = blockIdx.x * 256LL + threadIdx.x; e < n8; e += (long long)gridDim.x * 256) {
+    const float4 a = in[2 * e], b = in[2 * e + 1];
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x = v[j];
+      v[j] = 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+    }
+    out[e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                        pack_bf16x2(v[6], v[7]));
+  }
+}
+
+// Committed positions per canvas (adaptive stopping): one block per canvas,
+// a plain count of the commit mask's ones (integers: exact).
+__global__ void __launch_bounds__(256) count_committed_kernel(const uint8_t* __restrict__ mask, int canvas_len,
+                                                              int32_t* __restrict__ counts) {
+  __shared__ int total;
+  if (threadIdx.x == 0) total = 0;
+  __syncthreads();
+  const uint8_t* m = mask + (size_t)blockIdx.x * canvas_len;
+  int c = 0;
+  for (int i = threadIdx.x; i < canvas_len; i += blockDim.x) c += m[i] != 0 ? 1 : 0;
+  atomicAdd(&total, c);
+  __syncthreads();
+  if (threadIdx.x == 0) counts[blockIdx.x] = total;
+}
+
 // One thread waits, through the same bounded wait as every pipelined kernel,
 // on an mbarrier phase that nothing completes: after the wait limit it
 // records CANVAS_ERR_TIMEOUT in the status word and the kernel returns.
@@ -97,6 +131,21 @@ cudaError_t launch_cast_bf16(const float* in, void* out, long long n, cudaStream
   const long long n8 = n / 8;
   const int blocks = int(std::min<long long>((n8 + 255) / 256, 148LL * 16));
   cast_bf16_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gelu_bf16(const float* in, void* out, long long n, cudaStream_t stream) {
+  const long long n8 = n / 8;
+  const int blocks = int(std::min<long long>((n8 + 255) / 256, 148LL * 8));
+  gelu_bf16_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_committed(const uint8_t* mask, int n_canvas, int canvas_len, int32_t* counts,
+                                   cudaStream_t stream) {
+  count_committed_kernel<<<n_canvas, 256, 0, stream>>>(mask, canvas_len, counts);
   count_launches(1);
   return cudaGetLastError();
 }

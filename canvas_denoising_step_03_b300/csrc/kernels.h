@@ -59,7 +59,9 @@ struct GemmTcMaps {
 };
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 3;
 size_t gemm_tc_smem_bytes();
-cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStream_t stream);
+// reduce = false leaves a split product in its partials (g.partials[p],
+// [splits][M][N_p]) for a consumer that sums them in split order itself
+cudaError_t launch_gemm_tc(const GemmTcMaps& maps, const GemmTcArgs& g, cudaStream_t stream, bool reduce = true);
 
 // SIMT GEMM (fp32 path): C[M,N] = A[M,K] * op(B) (+C), TA/TB = float or bf16
 cudaError_t launch_gemm_simt(const void* A, const void* B, int b_mn_major, bool bf16, float* C, int M, int N,
@@ -85,9 +87,13 @@ cudaError_t launch_gemm_simt(const void* A, const void* B, int b_mn_major, bool 
 inline int attn_tail_rows(int C) { return 64 * ((C + 63 + 63) / 64 + 1); }
 
 struct PrologueArgs {
+  // the projections, or (splits > 1) the split-K partials of each: slice s
+  // of proj_x at proj_x + s * (B*C*N_x), summed in split order (s = 0, 1,
+  // ...) from 0 exactly as the GEMM's own reduce would
   const float* proj_q;  // [B*C, Hq*d]
   const float* proj_k;  // [B*C, Hkv*d]
   const float* proj_v;  // [B*C, Hkv*d] or null (global)
+  int splits;
   const float* gamma_q;
   const float* gamma_k;
   const float* freq;
@@ -124,6 +130,24 @@ struct KeyPrepArgs {
 };
 cudaError_t launch_key_prep(const KeyPrepArgs& k, bool bf16, cudaStream_t stream);
 
+// Block commit: the rows of a committed block written into the paged cache
+// at positions prefix_len[b] + i, then prefix_len[b] += C.
+struct KvAppendArgs {
+  const float* proj_k;       // [B*C, Hkv*d] x W_k^T
+  const float* proj_v;       // [B*C, Hkv*d] x W_v^T (sliding) or null
+  const float* gamma_k;
+  const float* freq;
+  int32_t* prefix_len;       // [B], advanced by C
+  void* k_pool;              // [num_pages][Hkv][page_tokens][d]: final keys (sliding) / raw r (global)
+  void* v_pool;              // values (sliding) or null
+  const int32_t* block_table;
+  int max_pages, page_tokens, num_pages;
+  int B, C, Hkv, d, max_prefix;  // max_prefix: positions must stay below it
+  float eps;
+  int global;
+};
+cudaError_t launch_kv_append(const KvAppendArgs& p, bool bf16, cudaStream_t stream);
+
 // CUDA-core attention (fp32 calls)
 struct AttnArgs {
   const void* Qp;            // [B][Hkv][G][C][d]
@@ -138,6 +162,7 @@ struct AttnArgs {
   const int32_t* prefix_len;
   int B, C, Hq, Hkv, d, max_prefix, window, Tpad;
   int global, v_unit_rms;
+  int causal;                // 1: encode mode, canvas row i sees canvas keys 0..i
   float scale;
   void* out;                 // [B][C][Hq*d]
   float* lse;                // [B][C][Hq] or null
@@ -150,6 +175,7 @@ constexpr int kAttnBN = 128;       // keys per block
 struct AttnTcArgs {
   int B, C, Hq, Hkv, G, d, DV, dv_parts, q_tiles, nsplit, max_prefix, window, Tpad;
   int kpre_paged;            // 1: prefix keys from the paged pool; 0: dense Kt
+  int causal;                // 1: encode mode, canvas row i sees canvas keys 0..i
   int pair;                  // 2: 4-SM kernel (two CTA pairs split the key blocks), head_dim 512;
                              // 0: one SM per 128-row tile
   const __nv_bfloat16* Qp;   // [B][Hkv][G][C][d] prepared queries (the 4-SM kernel reads half of each row)
@@ -176,6 +202,9 @@ cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream);
 cudaError_t launch_embed_input(const int32_t* tokens, const void* E, const float* soft, int rows, int D, int V,
                                void* x, float* x32, cudaStream_t stream);
 cudaError_t launch_cast_bf16(const float* in, void* out, long long n, cudaStream_t stream);
+cudaError_t launch_gelu_bf16(const float* in, void* out, long long n, cudaStream_t stream);
+cudaError_t launch_count_committed(const uint8_t* mask, int n_canvas, int canvas_len, int32_t* counts,
+                                   cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
 
 }  // namespace canvas

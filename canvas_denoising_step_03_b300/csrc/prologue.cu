@@ -121,6 +121,28 @@ __device__ __forceinline__ void load_row(const T* src, Row& r) {
   }
 }
 
+// A projection row summed over its split-K partials (slices `stride` floats
+// apart), in split order from 0: the same fp32 additions as the GEMM's own
+// split reduce, so the row is bit-identical to a reduced projection.
+template <int D>
+__device__ __forceinline__ void load_split_row(const float* src, size_t stride, int splits, Row& r) {
+  if (splits <= 1) {
+    load_row<float, D>(src, r);
+    return;
+  }
+  Row t;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerLane; ++k) r.lo[k] = r.hi[k] = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {
+    load_row<float, D>(src + sp * stride, t);
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      r.lo[k] += t.lo[k];
+      r.hi[k] += t.hi[k];
+    }
+  }
+}
+
 template <typename T, int D>
 __device__ __forceinline__ void store_row(T* dst, const Row& r) {
   using S = RowShape<D>;
@@ -261,14 +283,15 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
   const int t = P - (P & ~63) + i;       // tail row of this canvas token
 
   Row r;
+  const size_t M = (size_t)p.B * p.C;
   if (hh < p.Hq) {
     const int h = hh, hk = h / G, g = h % G;
-    load_row<float, D>(p.proj_q + (size_t)row * p.Hq * d + (size_t)h * d, r);
+    load_split_row<D>(p.proj_q + (size_t)row * p.Hq * d + (size_t)h * d, M * p.Hq * d, p.splits, r);
     norm_rope<D>(r, p.gamma_q, p.eps, p.freq, pos);
     store_row<T, D>(static_cast<T*>(p.Qp) + ((((size_t)b * p.Hkv + hk) * G + g) * p.C + i) * d, r);
   } else if (hh < p.Hq + p.Hkv) {
     const int hk = hh - p.Hq;
-    load_row<float, D>(p.proj_k + (size_t)row * p.Hkv * d + (size_t)hk * d, r);
+    load_split_row<D>(p.proj_k + (size_t)row * p.Hkv * d + (size_t)hk * d, M * p.Hkv * d, p.splits, r);
     const size_t trow = ((size_t)b * p.Hkv + hk) * p.Tpad + t;
     T* kdst = static_cast<T*>(p.Kx) + trow * d;
     if (p.global) {
@@ -281,7 +304,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueArgs p) {
     }
   } else {
     const int hk = hh - p.Hq - p.Hkv;
-    load_row<float, D>(p.proj_v + (size_t)row * p.Hkv * d + (size_t)hk * d, r);
+    load_split_row<D>(p.proj_v + (size_t)row * p.Hkv * d + (size_t)hk * d, M * p.Hkv * d, p.splits, r);
     store_row<T, D>(static_cast<T*>(p.Vx) + (((size_t)b * p.Hkv + hk) * p.Tpad + t) * d, r);
   }
 }
@@ -391,6 +414,68 @@ __global__ void __launch_bounds__(256, 2) key_prep_kernel(KeyPrepArgs k) {
   for (int w = w0; w < total; w += nwarps) key_prep_row<T, D>(k, w, k.max_prefix, k.Tpad);
 }
 
+// Block commit: one warp per (block row b*C + i, KV head), the row at
+// position prefix_len[b] + i written into its page.  Sliding layers: the final
+// key rotate(rms(k)) and the value; global layers: the raw shared projection
+// r.  Each row is computed in fp32 and stored once in T, exactly as the
+// prologue stores the same rows of a canvas.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs p) {
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int total = p.B * p.C * p.Hkv;
+  if (warp_global >= total) return;
+  const int lane = threadIdx.x & 31;
+  const int row = warp_global / p.Hkv;  // block row b*C + i
+  const int hk = warp_global % p.Hkv;
+  const int b = row / p.C, i = row % p.C;
+  const int P = p.prefix_len[b];
+  const int pos = P + i;
+  if (P < 0 || pos >= p.max_prefix) {
+    if (lane == 0) record_error(CANVAS_ERR_BOUNDS);
+    return;
+  }
+  const int lp = pos / p.page_tokens;
+  const int page = lp < p.max_pages ? p.block_table[(size_t)b * p.max_pages + lp] : -1;
+  if (page < 0 || page >= p.num_pages) {
+    if (lane == 0) record_error(CANVAS_ERR_BOUNDS);
+    return;
+  }
+  const size_t prow = ((size_t)page * p.Hkv + hk) * p.page_tokens + pos % p.page_tokens;
+  Row r;
+  load_row<float, D>(p.proj_k + (size_t)row * p.Hkv * D + (size_t)hk * D, r);
+  if (p.global) {
+    store_row<T, D>(static_cast<T*>(p.k_pool) + prow * D, r);
+    return;
+  }
+  norm_rope<D>(r, p.gamma_k, p.eps, p.freq, pos);
+  store_row<T, D>(static_cast<T*>(p.k_pool) + prow * D, r);
+  load_row<float, D>(p.proj_v + (size_t)row * p.Hkv * D + (size_t)hk * D, r);
+  store_row<T, D>(static_cast<T*>(p.v_pool) + prow * D, r);
+}
+
+// prefix_len[b] += C, after every row of the block has been written (a
+// separate launch: the append kernel reads prefix_len in every warp)
+__global__ void advance_prefix_kernel(int32_t* prefix_len, int B, int C) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) prefix_len[b] += C;
+}
+
+template <typename T>
+cudaError_t launch_kv_append_t(const KvAppendArgs& p, int blocks, cudaStream_t stream) {
+  switch (p.d) {
+    case 64: kv_append_kernel<T, 64><<<blocks, 256, 0, stream>>>(p); break;
+    case 128: kv_append_kernel<T, 128><<<blocks, 256, 0, stream>>>(p); break;
+    case 256: kv_append_kernel<T, 256><<<blocks, 256, 0, stream>>>(p); break;
+    case 512: kv_append_kernel<T, 512><<<blocks, 256, 0, stream>>>(p); break;
+    case 192: kv_append_kernel<T, 192><<<blocks, 256, 0, stream>>>(p); break;
+    case 320: kv_append_kernel<T, 320><<<blocks, 256, 0, stream>>>(p); break;
+    case 384: kv_append_kernel<T, 384><<<blocks, 256, 0, stream>>>(p); break;
+    case 448: kv_append_kernel<T, 448><<<blocks, 256, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_prologue_t(const PrologueArgs& p, int blocks, cudaStream_t stream) {
   if (sizeof(T) == 2 && (p.d & (p.d - 1)) != 0) return cudaErrorInvalidValue;
@@ -439,6 +524,18 @@ cudaError_t launch_key_prep_t(const KeyPrepArgs& k, long long blocks, cudaStream
 }
 
 }  // namespace
+
+cudaError_t launch_kv_append(const KvAppendArgs& p, bool bf16, cudaStream_t stream) {
+  if (bf16 && (p.d & (p.d - 1)) != 0) return cudaErrorInvalidValue;
+  const long long warps = (long long)p.B * p.C * p.Hkv;
+  const int blocks = int((warps * 32 + 255) / 256);
+  cudaError_t e = bf16 ? launch_kv_append_t<__nv_bfloat16>(p, blocks, stream) : launch_kv_append_t<float>(p, blocks, stream);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  advance_prefix_kernel<<<(p.B + 127) / 128, 128, 0, stream>>>(p.prefix_len, p.B, p.C);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prologue(const PrologueArgs& p, bool bf16, cudaStream_t stream) {
   const int heads = p.Hq + p.Hkv + (p.global ? 0 : p.Hkv);

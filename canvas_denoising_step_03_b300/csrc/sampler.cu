@@ -144,7 +144,7 @@ __device__ __forceinline__ void row_decision(const SampleArgs& a, int row, const
   a.entropy[row] = H;
   a.confidence[row] = conf;
   a.argmax[row] = t.bi;
-  if (a.commit_mode == 0) {
+  if ((a.commit_mode & 1) == 0) {
     const bool fr = a.frozen != nullptr && a.frozen[row] != 0;
     const bool commit = fr || (H < a.bound);
     int tok;
@@ -310,9 +310,11 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
     }
     s.bx = bv;
     s.bi = int(c0) + 8 * jb + e;
-    // (2) Z and T about the thread's maximum (base 2)
+    // (2) Z and T about the thread's maximum (base 2), two logits per
+    // packed fp32x2 instruction (even / odd positions in the two lanes)
     const float mt = bv * ysc;
-    float Z = 0.f, T = 0.f;
+    const uint64_t ysc2 = f2_pack(ysc, ysc), nmt2 = f2_pack(-mt, -mt);
+    uint64_t Z2 = 0, T2 = 0;
 #pragma unroll 4
     for (int k = 0; k < kMaxK; ++k) {
       const int j = int(threadIdx.x) + k * kThreads;
@@ -321,19 +323,16 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
         const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float t0 = fmaf(__uint_as_float(x4[q] << 16), ysc, -mt);
-          const float t1 = fmaf(__uint_as_float(x4[q] & 0xffff0000u), ysc, -mt);
-          const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-          Z += e0;
-          Z += e1;
-          T = fmaf(t0, e0, T);
-          T = fmaf(t1, e1, T);
+          const uint64_t t2 = f2_fma(f2_from_bf16x2(x4[q]), ysc2, nmt2);
+          const uint64_t e2 = f2_pack(ex2_approx(f2_lo(t2)), ex2_approx(f2_hi(t2)));
+          Z2 = f2_add(Z2, e2);
+          T2 = f2_fma(t2, e2, T2);
         }
       }
     }
     s.m = mt;
-    s.Z = Z;
-    s.T = T;
+    s.Z = f2_lo(Z2) + f2_hi(Z2);
+    s.T = f2_lo(T2) + f2_hi(T2);
   }
   // warp, then CTA, then cluster (every CTA merges the partial states in
   // rank order, so all end with the same bits)
@@ -379,15 +378,17 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
     }
     if (threadIdx.x == 0) {
       warp_part[0].m = t.m;
-      warp_part[0].Z = 1.0f / t.Z;
+      warp_part[0].Z = t.Z;
       if (rank == 0) row_decision(a, row, t);
     }
   }
   __syncthreads();
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  const RowState t = warp_part[0];  // m and 1 / Z
-  const float M = t.m;
-  const float invZ = t.Z;
+  const RowState t = warp_part[0];  // the row's m and Z
+  // p = 2^(y - m) / Z = 2^(y - (m + log2 Z)): the normaliser folded into the
+  // exponent (the fp32 rounding of m + log2 Z moves p by about 2^-19 relative)
+  const float nML = -(t.m + log2f(t.Z));
+  const uint64_t ysc2 = f2_pack(ysc, ysc), nML2 = f2_pack(nML, nML);
 #pragma unroll 4
   for (int k = 0; k < kMaxK; ++k) {
     const int j = int(threadIdx.x) + k * kThreads;
@@ -397,9 +398,10 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     float p[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      p[2 * j] = ex2_approx(fmaf(__uint_as_float(w[j] << 16), ysc, -M)) * invZ;
-      p[2 * j + 1] = ex2_approx(fmaf(__uint_as_float(w[j] & 0xffff0000u), ysc, -M)) * invZ;
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t t2 = f2_fma(f2_from_bf16x2(w[q]), ysc2, nML2);
+      p[2 * q] = ex2_approx(f2_lo(t2));
+      p[2 * q + 1] = ex2_approx(f2_hi(t2));
     }
     const long long o = (long long)row * a.V + c0 + i;
     if (a.probs_bf16) {
@@ -470,6 +472,78 @@ __global__ void __launch_bounds__(kThreads) sample_rows_kernel(SampleArgs a, con
   }
 }
 
+// Categorical draw for the committed positions (commit_mode bit 1): the
+// token is the smallest index k whose cumulative stored probability exceeds
+// u * (sum of the stored probabilities), u = the top 24 bits of the row's
+// SplitMix64 key / 2^24 (the key that would renoise the row: a position
+// either commits or renoises).  One block per row; thread t sums a contiguous
+// range in fp64, a block scan places the target, and the thread whose range
+// holds it walks its range in index order.  Frozen and renoised rows keep
+// their tokens.
+template <typename P>
+__device__ __forceinline__ double prob_at(const P* p, long long i);
+template <>
+__device__ __forceinline__ double prob_at<__nv_bfloat16>(const __nv_bfloat16* p, long long i) {
+  return double(__bfloat162float(p[i]));
+}
+template <>
+__device__ __forceinline__ double prob_at<float>(const float* p, long long i) {
+  return double(p[i]);
+}
+
+template <typename P>
+__global__ void __launch_bounds__(256) categorical_kernel(SampleArgs a, const P* __restrict__ probs) {
+  constexpr int kT = 256;
+  __shared__ double part[kT];
+  __shared__ double target;
+  __shared__ int found;
+  const int row = blockIdx.x;
+  if (a.commit_mask[row] == 0) return;
+  if (a.frozen != nullptr && a.frozen[row] != 0) return;
+  const P* pr = probs + (long long)row * a.V;
+  const int n = (a.V + kT - 1) / kT;
+  const long long i0 = (long long)threadIdx.x * n;
+  const long long i1 = min((long long)a.V, i0 + n);
+  double sum = 0.0;
+  for (long long i = i0; i < i1; ++i) sum += prob_at<P>(pr, i);
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // exclusive prefix of the range sums, in thread (index) order
+    double acc = 0.0;
+    for (int t = 0; t < kT; ++t) {
+      const double v = part[t];
+      part[t] = acc;
+      acc += v;
+    }
+    const uint64_t key = renoise_key(a.seed, a.step, uint32_t(row));
+    target = double(key >> 40) * (1.0 / 16777216.0) * acc;
+    found = -1;
+  }
+  __syncthreads();
+  const double lo = part[threadIdx.x];
+  const double hi = threadIdx.x + 1 < kT ? part[threadIdx.x + 1] : lo + sum;
+  if (lo <= target && target < hi) {
+    // the ranges are disjoint, so exactly one thread gets here
+    double run = lo;
+    int k = -1, last = -1;
+    for (long long i = i0; i < i1; ++i) {
+      const double v = prob_at<P>(pr, i);
+      run += v;
+      if (v > 0.0) last = int(i);
+      if (run > target) {
+        k = int(i);
+        break;
+      }
+    }
+    // the walk's sum ends an ulp short of hi: the target sits on the range's
+    // last boundary, which its last positive entry closes
+    found = k >= 0 ? k : last;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.tokens[row] = found >= 0 ? found : a.argmax[row];
+}
+
 // Left-prefix commit mode: one thread per canvas walks its rows in order.
 __global__ void commit_prefix_kernel(SampleArgs a, int n_canvas) {
   const int cv = blockIdx.x * blockDim.x + threadIdx.x;
@@ -531,9 +605,18 @@ cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, c
   }
   if (e != cudaSuccess) return e;
   count_launches(1);
-  if (a.commit_mode == 1) {
+  if (a.commit_mode & 1) {
     const int n_canvas = a.rows / a.canvas_len;
     commit_prefix_kernel<<<(n_canvas + 127) / 128, 128, 0, stream>>>(a, n_canvas);
+    e = cudaGetLastError();
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.commit_mode & 2) {
+    if (bf16)
+      categorical_kernel<__nv_bfloat16><<<a.rows, 256, 0, stream>>>(a, a.probs_bf16);
+    else
+      categorical_kernel<float><<<a.rows, 256, 0, stream>>>(a, a.probs_f32);
     e = cudaGetLastError();
     count_launches(1);
   }

@@ -24,9 +24,10 @@ import numpy as np
 import torch
 
 from . import (CANVAS_BF16, CANVAS_LAYER_GLOBAL, CANVAS_LAYER_SLIDING, canvas_attention,
-               canvas_attention_workspace_size, canvas_cast_bf16, canvas_embed_input, canvas_gemm_bf16,
-               canvas_gemm_bf16_to_bf16, canvas_gemm_workspace_size, canvas_sample, canvas_sample_workspace_size,
-               make_kv_cache, workspace)
+               canvas_attention_workspace_size, canvas_cast_bf16, canvas_count_committed, canvas_embed_input,
+               canvas_gelu_bf16, canvas_gemm_bf16, canvas_gemm_bf16_to_bf16, canvas_gemm_workspace_size,
+               canvas_sample,
+               canvas_sample_workspace_size, canvas_temperature_at, make_kv_cache, workspace)
 
 
 def _bf16(a: np.ndarray, device) -> torch.Tensor:
@@ -38,7 +39,14 @@ class CanvasLoop:
     ``canvas_workloads.LoopInputs``: bf16 bit patterns, caches holding
     positions cache_lo .. prefix-1 of every sequence)."""
 
-    def __init__(self, inp, device="cuda", page_tokens: int = 64, seed_pages: int = 1234):
+    def __init__(self, inp, device="cuda", page_tokens: int = 64, seed_pages: int = 1234, schedule=None,
+                 categorical: bool = False):
+        """``schedule`` = (t_max, t_min, steps): the sampler temperature of
+        step s is canvas_temperature_at(s, steps, t_max, t_min) (default: 1);
+        ``categorical``: committed positions take a categorical draw from
+        their probabilities instead of the argmax."""
+        self.schedule = schedule
+        self.commit_mode = 2 if categorical else 0
         import canvas_workloads as wl  # shapes and page tables of the seeded inputs
         cfg = inp.cfg
         self.cfg, self.dev = cfg, device
@@ -81,11 +89,36 @@ class CanvasLoop:
                   [canvas_gemm_workspace_size(R, V, D)])
         self.gemm_ws = workspace(gws, device)
         self.samp_ws = workspace(canvas_sample_workspace_size(CANVAS_BF16, R, V, D), device)
+        self.counts = torch.zeros(B, dtype=torch.int32, device=device)
+        # self-conditioning MLP (optional): sc = W2 bf16(gelu(W1 bf16(soft)))
+        self.sc = None
+        if getattr(inp, "sc_W1", None) is not None:
+            H = inp.sc_W1.shape[0]
+            self.sc = dict(W1=_bf16(inp.sc_W1, device), W2=_bf16(inp.sc_W2, device),
+                           s16=torch.empty((R, D), dtype=torch.bfloat16, device=device),
+                           h=torch.empty((R, H), dtype=torch.float32, device=device),
+                           g=torch.empty((R, H), dtype=torch.bfloat16, device=device),
+                           out=torch.empty((R, D), dtype=torch.float32, device=device))
+            gws2 = max(canvas_gemm_workspace_size(R, H, D), canvas_gemm_workspace_size(R, D, H))
+            if gws2 > self.gemm_ws.numel():
+                self.gemm_ws = workspace(gws2, device)
         self.step_index = 0
 
     # ---- the stages of a step (each one C-ABI call or two)
+    def selfcond(self, soft: torch.Tensor) -> torch.Tensor:
+        """The self-conditioning MLP on the previous soft embedding (fp32 out)."""
+        s = self.sc
+        canvas_cast_bf16(soft, s["s16"])
+        canvas_gemm_bf16(s["s16"], s["W1"], 0, s["h"], 0, self.gemm_ws)
+        canvas_gelu_bf16(s["h"], s["g"])
+        canvas_gemm_bf16(s["g"], s["W2"], 0, s["out"], 0, self.gemm_ws)
+        return s["out"]
+
     def embed(self, tokens: torch.Tensor, soft):
-        """x, x32 = E[tokens] + soft (soft None: no self-conditioning input)."""
+        """x, x32 = E[tokens] + soft (soft None: no self-conditioning input);
+        with the self-conditioning MLP, soft passes through it first."""
+        if soft is not None and self.sc is not None:
+            soft = self.selfcond(soft)
         canvas_embed_input(tokens, self.E, soft, self.x, self.x32)
 
     def attention(self, k: int, x: torch.Tensor) -> torch.Tensor:
@@ -113,9 +146,32 @@ class CanvasLoop:
         """The sampler of step ``step``; outputs in next_tokens, mask, entropy,
         conf, argmax, soft."""
         cfg = self.cfg
-        canvas_sample(logits, self.E, cfg.bound, cfg.seed, step, 1.0, 0, cfg.C, frozen, frozen_tokens,
-                      self.next_tokens, self.mask, self.entropy, self.conf, self.argmax, None, CANVAS_BF16,
-                      self.soft, self.samp_ws)
+        canvas_sample(logits, self.E, cfg.bound, cfg.seed, step, self.temperature(step), self.commit_mode, cfg.C,
+                      frozen, frozen_tokens, self.next_tokens, self.mask, self.entropy, self.conf, self.argmax, None,
+                      CANVAS_BF16, self.soft, self.samp_ws)
+
+    def temperature(self, step: int) -> float:
+        if self.schedule is None:
+            return 1.0
+        t_max, t_min, steps = self.schedule
+        return canvas_temperature_at(step, steps, t_max, t_min)
+
+    def committed_counts(self) -> torch.Tensor:
+        """Committed positions of each canvas after the last step (device)."""
+        canvas_count_committed(self.mask, self.cfg.C, self.counts)
+        return self.counts
+
+    def run(self, max_steps: int, stop_when_committed: bool = True) -> int:
+        """Steps until every canvas is fully committed (adaptive stopping) or
+        max_steps; returns the number of steps run.  The stop test reads the
+        per-canvas counts back to the host after each step."""
+        for n in range(max_steps):
+            self.step()
+            if stop_when_committed:
+                counts = self.committed_counts().cpu().numpy()   # device -> host copy, host-side test
+                if bool(np.all(counts == self.cfg.C)):
+                    return n + 1
+        return max_steps
 
     def step(self, keep_attn: bool = False, mark=None):
         """Run one denoising step on the loop's own state; returns the

@@ -303,6 +303,7 @@ class LoopConfig:
     n_global: int = 1
     bound: float = 0.3
     E_std: float = 0.02
+    selfcond_hidden: int = 0   # > 0: the self-conditioning MLP's hidden width (0: P.E enters as it is)
 
     def layer_cfgs(self):
         out = []
@@ -313,21 +314,21 @@ class LoopConfig:
         return out
 
 
-def loop_config(prefix: int, B: int = 4, steps: int = 48) -> LoopConfig:
+def loop_config(prefix: int, B: int = 4, steps: int = 48, selfcond_hidden: int = 0) -> LoopConfig:
     """The batched loop: 4 canvases of 256, 5 sliding layers (the sliding-layer
     shapes) and 1 global layer (the global-layer shapes), vocab 262144."""
     return LoopConfig(f"loop_p{prefix}", B=B, C=256, prefix=prefix, steps=steps, V=262144, D=2816, seed=11,
-                      sliding=SLIDING, global_=GLOBAL)
+                      sliding=SLIDING, global_=GLOBAL, selfcond_hidden=selfcond_hidden)
 
 
-def mini_loop_config(steps: int = 4) -> LoopConfig:
+def mini_loop_config(steps: int = 4, selfcond_hidden: int = 0) -> LoopConfig:
     """A small loop of the same structure for step-by-step parity."""
     sl = AttnConfig("mini-sliding", B=2, C=32, prefix=(160,), D=256, Hq=4, Hkv=2, d=64, layer="sliding",
                     window=48, theta=1e4, rotary_fraction=1.0, dtype="bf16", seed=0)
     gl = AttnConfig("mini-global", B=2, C=32, prefix=(160,), D=256, Hq=4, Hkv=1, d=128, layer="global",
                     window=0, theta=1e6, rotary_fraction=0.25, dtype="bf16", seed=0)
     return LoopConfig("mini_loop", B=2, C=32, prefix=160, steps=steps, V=4096, D=256, seed=21, sliding=sl,
-                      global_=gl, bound=0.3, E_std=0.3)
+                      global_=gl, bound=0.3, E_std=0.3, selfcond_hidden=selfcond_hidden)
 
 
 @dataclass
@@ -351,6 +352,8 @@ class LoopInputs:
     layers: list
     E: np.ndarray            # [V, D]
     tokens0: np.ndarray      # int32 [B*C]
+    sc_W1: Optional[np.ndarray] = None   # [H, D] self-conditioning MLP (bf16 bits), or None
+    sc_W2: Optional[np.ndarray] = None   # [D, H]
 
 
 def make_loop_inputs(cfg: LoopConfig) -> LoopInputs:
@@ -384,7 +387,14 @@ def make_loop_inputs(cfg: LoopConfig) -> LoopInputs:
     rng = np.random.default_rng(cfg.seed)
     E = rng.standard_normal((cfg.V, cfg.D), dtype=np.float32) * np.float32(cfg.E_std)
     tokens0 = rng.integers(0, cfg.V, size=cfg.B * cfg.C).astype(np.int32)
-    return LoopInputs(cfg=cfg, layers=layers, E=_store(E, "bf16"), tokens0=tokens0)
+    W1 = W2 = None
+    if cfg.selfcond_hidden > 0:
+        # a separate stream, so the other draws do not depend on it
+        r2 = np.random.default_rng(cfg.seed + 7919)
+        H = cfg.selfcond_hidden
+        W1 = _store(r2.standard_normal((H, cfg.D), dtype=np.float32) * np.float32(1.0 / np.sqrt(cfg.D)), "bf16")
+        W2 = _store(r2.standard_normal((cfg.D, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H)), "bf16")
+    return LoopInputs(cfg=cfg, layers=layers, E=_store(E, "bf16"), tokens0=tokens0, sc_W1=W1, sc_W2=W2)
 
 
 def page_layout_range(B: int, lo: int, hi: int, page_tokens: int, seed: int = 1234, spare_pages: int = 2):

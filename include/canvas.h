@@ -152,6 +152,66 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D,
                                void* out, float* lse,
                                void* workspace, size_t ws_bytes, canvas_stream_t stream);
 
+/*
+ * canvas_attention_encode -- the same layer in encode mode.
+ *
+ * Defined by [AIT] "섹션별 상세", the decode / encode paragraph: committed
+ * tokens are encoded causally, like a prefill.  Every argument, layout, error
+ * and the workspace are those of canvas_attention; the one difference is the
+ * mask inside the block: row i attends to the visible committed prefix (as in
+ * decode mode) and to block rows 0 .. i only.  A caller that commits a
+ * finished canvas runs its layers in this mode and appends each layer's rows
+ * to the cache with canvas_kv_append.
+ */
+canvas_status canvas_attention_encode(const void* x, int dtype, int B, int C, int D,
+                                      const void* W_q, const void* W_k, const void* W_v,
+                                      int Hq, int Hkv, int d,
+                                      const float* gamma_q, const float* gamma_k, float eps,
+                                      const float* freq, int layer_type,
+                                      const canvas_kv_cache* kv,
+                                      const int32_t* prefix_len, int max_prefix, int window,
+                                      float scale, int v_unit_rms,
+                                      void* out, float* lse,
+                                      void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
+/* Workspace (bytes) that canvas_kv_append needs; 0 for an invalid shape. */
+size_t canvas_kv_append_workspace_size(int dtype, int B, int C, int D, int Hkv, int d, int layer_type);
+
+/*
+ * canvas_kv_append -- block commit: write a committed block's cache rows.
+ *
+ * Defined by [AB] "블록 자동 회귀 노이즈 제거 및 자체 수정" (a denoised block is
+ * committed to the KV cache) and [AIT] "섹션별 상세" (the attention-block
+ * snippet: keys are normed and rotated, values are not; on full-attention
+ * layers W_v = W_k and only K is normed and rotated).  Block row i of
+ * sequence b is written at position p = prefix_len[b] + i:
+ *   sliding layers  k_pool <- rotate(rms(x W_k^T, gamma_k)) at position p,
+ *                   v_pool <- x W_v^T   (the final keys and values)
+ *   global layers   k_pool <- r = x W_k^T (the raw shared row; its key is
+ *                   formed from it at attention time)
+ * each computed in fp32 and stored once in the call's dtype, exactly as
+ * canvas_attention stores the same rows of a canvas; then prefix_len[b] += C
+ * (on the device, after every row is written).
+ *
+ *   x        [B, C, D] dtype      the block's layer input, 16-byte aligned
+ *   W_k, W_v [Hkv*d, D] dtype     W_v NULL on global layers
+ *   gamma_k [d], freq [d/2] fp32, eps, layer_type: as for canvas_attention
+ *   kv       host pointer to the cache descriptor; its pools are WRITTEN.
+ *            The block table must map every page the new positions fall in.
+ *   prefix_len [B] int32 device   read, then advanced by C
+ *   max_prefix                    host: every new position must be below it
+ *                                 and kv must be able to hold it; a row past
+ *                                 it, or on an unmapped page, is skipped and
+ *                                 records CANVAS_ERR_BOUNDS
+ *   workspace, ws_bytes           >= canvas_kv_append_workspace_size(...)
+ * Asynchronous on `stream`.
+ */
+canvas_status canvas_kv_append(const void* x, int dtype, int B, int C, int D,
+                               const void* W_k, const void* W_v, int Hkv, int d,
+                               const float* gamma_k, float eps, const float* freq, int layer_type,
+                               const canvas_kv_cache* kv, int32_t* prefix_len, int max_prefix,
+                               void* workspace, size_t ws_bytes, canvas_stream_t stream);
+
 /* Workspace (bytes) that canvas_sample needs; 0 for an invalid shape. */
 size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
 
@@ -170,9 +230,18 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  *   seed, step                    renoise key = m(m(m(seed) ^ step) ^ row),
  *                                 m = one SplitMix64 output; token = key mod V
  *   temperature                   logits are divided by it (> 0)
- *   commit_mode                   0: per position; 1: the longest run of
- *                                 qualifying positions from the left of each
- *                                 canvas of canvas_len rows
+ *   commit_mode                   bit 0 -- 0: commit per position; 1: the
+ *                                 longest run of qualifying positions from
+ *                                 the left of each canvas of canvas_len rows.
+ *                                 bit 1 -- 0: a committed (not frozen)
+ *                                 position takes its argmax; 1: it takes a
+ *                                 categorical draw from its stored
+ *                                 probabilities p~ (the tempered softmax in
+ *                                 the probability dtype below): the smallest k
+ *                                 with sum_{j<=k} p~_j > u * sum_j p~_j, sums in
+ *                                 fp64, u = (key >> 40) / 2^24 with key the
+ *                                 row's renoise key (one key per row: a
+ *                                 position either commits or renoises)
  *   canvas_len                    C (rows % C == 0 in mode 1)
  *   frozen   [rows] uint8 or NULL       1: position already committed; it keeps
  *   frozen_tokens [rows] int32 or NULL  its token and counts as committed
@@ -259,6 +328,38 @@ canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const flo
  * the bf16 operands of the next call.
  */
 canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stream_t stream);
+
+/*
+ * canvas_gelu_bf16 -- out[i] = bf16(gelu(in[i])), GELU in its tanh form
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated in fp32 and
+ * rounded once (nearest even); n % 8 == 0, both 16-byte aligned.  Glue: the
+ * activation of the self-conditioning MLP ([AIT] glossary, self-conditioning:
+ * the expected embedding P.E passes through a small MLP that maps zero to
+ * zero before it is added to the canvas input), built as
+ *   sc = W_2 . bf16(gelu(W_1 . bf16(soft_emb)))   (canvas_cast_bf16,
+ *   canvas_gemm_bf16, canvas_gelu_bf16, canvas_gemm_bf16; no biases).
+ */
+canvas_status canvas_gelu_bf16(const float* in, void* out, size_t n, canvas_stream_t stream);
+
+/*
+ * canvas_count_committed -- committed positions of each canvas, for adaptive
+ * stopping ("[논문리뷰] DiffusionGemma Technical Report" §1: the loop stops
+ * once every position of the canvas is committed).
+ *   commit_mask [rows] uint8 (canvas_sample's output), rows % canvas_len == 0
+ *   counts [rows / canvas_len] int32 out: ones of each canvas's mask
+ * Asynchronous on `stream`; the caller reads counts back to decide.
+ */
+canvas_status canvas_count_committed(const uint8_t* commit_mask, int rows, int canvas_len, int32_t* counts,
+                                     canvas_stream_t stream);
+
+/*
+ * canvas_temperature_at -- host helper: the sampler temperature of denoising
+ * step `step` of `steps` on a linear schedule from t_max (step 0) to t_min
+ * (step steps - 1), [AIT] "섹션별 상세", sampling-loop paragraph (the
+ * temperature falls from t_max to t_min over max_denoising_steps).  Pass the
+ * result as canvas_sample's temperature.  steps <= 1 gives t_max.
+ */
+float canvas_temperature_at(int step, int steps, float t_max, float t_min);
 
 /*
  * canvas_selftest_wait_timeout -- diagnostic; the method has no counterpart.

@@ -163,8 +163,12 @@ def _row_slack(q, dq, abs_keys_hi, abs_dkeys, vals, abs_dvals, p, o, scale):
 def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma_k,
                      eps: float, freq, layer: str, cache_k, cache_v, prefix_len, window: int,
                      scale: float = 1.0, v_unit_rms: bool = False, storage: str = "fp64",
-                     rows: Optional[Iterable] = None, slack_eps: Optional[float] = None):
-    """Decode-mode canvas attention for one layer.
+                     rows: Optional[Iterable] = None, slack_eps: Optional[float] = None,
+                     causal: bool = False, cache_dk=None, cache_dv=None):
+    """Canvas attention for one layer: decode mode, or encode mode with
+    ``causal`` ([AIT] §섹션별 상세, the decode / encode paragraph: encoding the
+    committed tokens is causal, like a prefill -- canvas row i sees the
+    canvas keys j <= i, and the committed prefix as in decode mode).
 
     Arguments are exact fp64 values (the stored inputs widened).  Shapes:
     x [B, C, D]; W_q [Hq*d, D]; W_k, W_v [Hkv*d, D] (W_v None on global
@@ -175,7 +179,10 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
     normaliser of each softmax row.  ``rows`` optionally restricts the work to
     a list of (b, h, i) triples; the other entries are NaN.  With
     ``slack_eps`` (bf16 storage only) a third array [B, C, Hq*d] holds the
-    rounding slack of every output element (module docstring).
+    rounding slack of every output element (module docstring);
+    ``cache_dk`` / ``cache_dv`` (same shapes as the caches, or None) then give
+    the flip of every cached element that was itself a rounding tie when it
+    was stored (rows appended by ``kv_append``), 0 elsewhere.
     """
     x = np.asarray(x, np.float64)
     B, C, D = x.shape
@@ -221,7 +228,8 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                 vp = np.asarray(cache_v[b, hk, :P], np.float64)
                 kc, dkc = _store(rotate(rms(k_raw[b, hk], gamma_k, eps), freq, P), storage, sl_eps)
                 vc, dvc = _store(v_raw[b, hk], storage, sl_eps)
-                dkp, dvp = zeros_like(kp), zeros_like(vp)
+                dkp = zeros_like(kp) if cache_dk is None else np.abs(np.asarray(cache_dk[b, hk, :P], np.float64))
+                dvp = zeros_like(vp) if cache_dv is None else np.abs(np.asarray(cache_dv[b, hk, :P], np.float64))
             else:
                 rp = np.asarray(cache_k[b, hk, :P], np.float64)
                 rc, drc = _store(k_raw[b, hk], storage, sl_eps)
@@ -236,15 +244,17 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     vv = r
                 vp, vc = vv[:P], vv[P:]
                 if want_slack:
-                    # a flip of a canvas r element moves that row's key (through
-                    # rms and rotate: at most |gamma_k| s (|dr_t| + |dr_pair|))
-                    # and its value (dr itself, or its unit-RMS image)
-                    nr = np.sqrt(np.sum(rc * rc, -1, keepdims=True))
+                    # a flip of a stored r element (a canvas row, or a cached
+                    # row that was a tie when appended) moves that row's key
+                    # (through rms and rotate: at most |gamma_k| s (|dr_t| +
+                    # |dr_pair|)) and its value (dr itself, or its unit-RMS image)
+                    drp = np.zeros_like(rp) if cache_dk is None else np.asarray(cache_dk[b, hk, :P], np.float64)
+                    dr = np.abs(np.concatenate([drp, drc], axis=0))
+                    nr = np.sqrt(np.sum(r * r, -1, keepdims=True))
                     s_row = np.sqrt(d) / (nr + eps)
-                    prop = np.max(np.abs(gamma_k)) * s_row * (np.abs(drc) + np.abs(_pair_partner(drc)))
-                    dkk = np.abs(dkk)
-                    dkk[P:] += prop * 1.01
-                    dvv = np.concatenate([np.zeros_like(rp), np.abs(drc) * (s_row * 1.01 if v_unit_rms else 1.0)])
+                    prop = np.max(np.abs(gamma_k)) * s_row * (dr + _pair_partner(dr))
+                    dkk = np.abs(dkk) + prop * 1.01
+                    dvv = dr * (s_row * 1.01 if v_unit_rms else 1.0)
                     dkp, dkc = dkk[:P], dkk[P:]
                     dvp, dvc = dvv[:P], dvv[P:]
             # the keys of this head in position order, from the first prefix
@@ -266,8 +276,10 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     vis = visible_prefix(P, i, window, layer)
                     assert vis.stop == P and vis.start >= lo
                     j0 = vis.start - lo
-                    keys = keys_all[j0:]
-                    vals = vals_all[j0:]
+                    # canvas keys 0 .. C-1 (decode) or 0 .. i (encode)
+                    j1 = (P - lo) + (i + 1 if causal else C)
+                    keys = keys_all[j0:j1]
+                    vals = vals_all[j0:j1]
                     s = scale * (keys @ q[h, i])
                     m = np.max(s)
                     e = np.exp(s - m)
@@ -276,12 +288,54 @@ def canvas_attention(x, W_q, W_k, W_v, Hq: int, Hkv: int, d: int, gamma_q, gamma
                     out[b, i, h * d:(h + 1) * d] = o
                     lse[b, i, h] = m + np.log(Z)
                     if want_slack:
-                        slack[b, i, h * d:(h + 1) * d] = _row_slack(q[h, i], dq[h, i], abs_k_hi_all[j0:],
-                                                                    abs_dk_all[j0:], vals, abs_dv_all[j0:],
+                        slack[b, i, h * d:(h + 1) * d] = _row_slack(q[h, i], dq[h, i], abs_k_hi_all[j0:j1],
+                                                                    abs_dk_all[j0:j1], vals, abs_dv_all[j0:j1],
                                                                     e / Z, o, scale)
     if want_slack:
         return out, lse, slack
     return out, lse
+
+
+def kv_append(x, W_k, W_v, Hkv: int, d: int, gamma_k, eps: float, freq, layer: str, prefix_len,
+              storage: str = "bf16", slack_eps: Optional[float] = None):
+    """The cache rows a committed block adds ([AIT] §섹션별 상세, the decode /
+    encode paragraph and the attention-block snippet; [AB] §블록 자동 회귀
+    노이즈 제거 및 자체 수정: the denoised block is committed to the KV cache).
+
+    Block row i of sequence b sits at position prefix_len[b] + i.  Sliding
+    layers keep final keys and values: k = rotate(rms(x W_k^T, gamma_k)) at
+    that position, v = x W_v^T.  Global layers keep the raw shared projection
+    r = x W_k^T (its key is formed from it at attention time).  Each row is
+    rounded to bf16 where it is stored (``storage='bf16'``).
+
+    Returns (k_rows, v_rows or None) [B, Hkv, C, d]; with ``slack_eps`` also
+    the flip deltas of the rows (0 where the rounding is not a tie).
+    """
+    x = np.asarray(x, np.float64)
+    B, C, D = x.shape
+
+    def heads(z):
+        return z.reshape(B, C, Hkv, d).transpose(0, 2, 1, 3)
+
+    k_raw = heads(x @ np.asarray(W_k, np.float64).T)
+    sl = slack_eps if storage == "bf16" else None
+    if layer == "global":
+        kr, dk = _store(k_raw, storage, sl)
+        return (kr, None, dk, None) if sl is not None else (kr, None)
+    v_raw = heads(x @ np.asarray(W_v, np.float64).T)
+    ks, dks, vs, dvs = [], [], [], []
+    for b in range(B):
+        P = int(prefix_len[b])
+        kb, dkb = _store(rotate(rms(k_raw[b], gamma_k, eps), freq, P), storage, sl)
+        vb, dvb = _store(v_raw[b], storage, sl)
+        ks.append(kb)
+        vs.append(vb)
+        dks.append(dkb)
+        dvs.append(dvb)
+    k, v = np.stack(ks), np.stack(vs)
+    if sl is not None:
+        return k, v, np.stack(dks), np.stack(dvs)
+    return k, v
 
 
 def visible_pairs(C: int, P: int, window: int, layer: str) -> int:

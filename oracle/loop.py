@@ -25,8 +25,18 @@ from typing import Iterable, Optional
 import numpy as np
 
 from .attention import canvas_attention
-from .numerics import bf16_round
+from .numerics import bf16_round, gelu_tanh
 from .sampler import canvas_sample
+
+
+def selfcond_mlp(soft: np.ndarray, W1: np.ndarray, W2: np.ndarray) -> np.ndarray:
+    """The self-conditioning MLP on the previous step's soft embedding ([AIT]
+    glossary, self-conditioning: P.E passes through a small MLP, which maps
+    zero to zero, before it is added to the canvas input):
+    W2 bf16(gelu(W1 bf16(soft))), no biases, the rounding points of the path
+    (bf16 GEMM operands) mirrored; W1 [H, D], W2 [D, H] exact values."""
+    h = bf16_round(soft) @ np.asarray(W1, np.float64).T
+    return bf16_round(gelu_tanh(h)) @ np.asarray(W2, np.float64).T
 
 
 def dense_cache(rows: np.ndarray, lo: int, prefix: int) -> np.ndarray:
@@ -40,7 +50,8 @@ def dense_cache(rows: np.ndarray, lo: int, prefix: int) -> np.ndarray:
 
 def loop_step(layers, E: np.ndarray, tokens: np.ndarray, soft_prev: Optional[np.ndarray], step: int, B: int,
               C: int, seed: int, bound: float, frozen=None, frozen_tokens=None,
-              sample_rows: Optional[Iterable[int]] = None, slack_eps: Optional[float] = None):
+              sample_rows: Optional[Iterable[int]] = None, slack_eps: Optional[float] = None,
+              selfcond=None):
     """One step.  ``layers``: dicts of exact fp64 layer inputs (keys W_q, W_k,
     W_v, W_o, gamma_q, gamma_k, freq, eps, Hq, Hkv, d, layer, window,
     cache_k, cache_v [dense by position], prefix).  Returns a dict with the
@@ -49,13 +60,14 @@ def loop_step(layers, E: np.ndarray, tokens: np.ndarray, soft_prev: Optional[np.
     stored, ``attn_exact``: before that rounding; [B, C, Hq*d]) and, with
     ``slack_eps``, their rounding slack; the bf16 logits (all rows, or only
     ``sample_rows`` -- NaN elsewhere) and the sampler outputs of those rows
-    (soft_emb for them)."""
+    (soft_emb for them).  ``selfcond`` = (W1, W2): the previous soft
+    embedding enters through ``selfcond_mlp`` (default: as it is)."""
     rows = B * C
     D = E.shape[1]
     sel = np.arange(rows) if sample_rows is None else np.asarray(sorted(set(sample_rows)), np.int64)
     v = E[np.asarray(tokens, np.int64)]
     if soft_prev is not None:
-        v = v + soft_prev
+        v = v + (soft_prev if selfcond is None else selfcond_mlp(soft_prev, *selfcond))
     x = v.copy()
     xs, outs, exact, slacks = [x.copy()], [], [], []
     for L in layers:

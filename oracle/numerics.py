@@ -71,3 +71,12 @@ def rotate(x: np.ndarray, freq: np.ndarray, start) -> np.ndarray:
     pos = np.arange(L, dtype=np.float64)[:, None] + np.asarray(start, dtype=np.float64)
     ang = pos * f2
     return np.cos(ang) * x + np.sin(ang) * companion
+
+
+def gelu_tanh(x) -> np.ndarray:
+    """GELU in its tanh form, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
+    fp64 -- the activation taken for the self-conditioning MLP ([AIT]
+    glossary, self-conditioning: "a small MLP" that maps zero to zero; the
+    pages name no activation, and this is the Gemma family's)."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))

@@ -14,6 +14,12 @@ What is computed ([AIT] §섹션별 상세, the sampling-loop paragraph; [AB]
 4. self-conditioning soft embedding: soft_emb = P E, the probability-weighted
    embedding of every position.
 
+Variants ([AIT] §섹션별 상세, sampling-loop paragraph: the temperature falls
+from t_max to t_min over max_denoising_steps; a committed token is drawn from
+the tempered softmax; "[논문리뷰] DiffusionGemma Technical Report" §1: adaptive
+stopping once every position is committed): ``temperature_schedule``,
+``categorical=True`` and ``all_committed``.
+
 Readings (listed in the design notes): the commit test is strict, H < bound,
 per position (``commit_mode=0``); ``commit_mode=1`` instead commits the longest
 run of qualifying positions from the left of each canvas (the page's "fix the
@@ -30,7 +36,40 @@ from typing import Iterable, Optional
 import numpy as np
 
 from .numerics import bf16_round
-from .splitmix import renoise_token
+from .splitmix import key_uniform, renoise_key, renoise_token
+
+
+def temperature_schedule(step: int, steps: int, t_max: float, t_min: float) -> float:
+    """Temperature of denoising step ``step`` of ``steps``: linear from t_max
+    (step 0) to t_min (step steps - 1); one step, or a step before 0, is t_max."""
+    if steps <= 1 or step <= 0:
+        return float(t_max)
+    if step >= steps - 1:
+        return float(t_min)
+    return float(t_max) + (float(t_min) - float(t_max)) * step / (steps - 1)
+
+
+def categorical_token(stored_row: np.ndarray, u: float) -> int:
+    """The inverse-CDF draw from one row of stored probabilities: the
+    smallest k with cumsum(p)[k] > u * sum(p) (cumulative sums in fp64, index
+    order; the stored row need not sum to exactly 1)."""
+    c = np.cumsum(np.asarray(stored_row, np.float64))
+    target = u * c[-1]
+    return int(np.searchsorted(c, target, side="right"))
+
+
+def categorical_margin(stored_row: np.ndarray, u: float) -> float:
+    """Distance of the draw's target from the nearest cumulative boundary,
+    relative to the row total (a tie when it is tiny)."""
+    c = np.cumsum(np.asarray(stored_row, np.float64))
+    target = u * c[-1]
+    return float(np.min(np.abs(c - target)) / c[-1])
+
+
+def all_committed(commit_mask: np.ndarray, canvas_len: int) -> np.ndarray:
+    """Adaptive stopping: per canvas, whether every position is committed."""
+    m = np.asarray(commit_mask).reshape(-1, canvas_len)
+    return np.all(m != 0, axis=1)
 
 
 def row_statistics(logits_row: np.ndarray, temperature: float = 1.0):
@@ -50,7 +89,7 @@ def row_statistics(logits_row: np.ndarray, temperature: float = 1.0):
 def canvas_sample(logits, E, entropy_bound: float, seed: int, step: int,
                   temperature: float = 1.0, commit_mode: int = 0, canvas_len: Optional[int] = None,
                   frozen=None, frozen_tokens=None, probs_storage: str = "fp64",
-                  soft_rows: Optional[Iterable[int]] = None):
+                  soft_rows: Optional[Iterable[int]] = None, categorical: bool = False):
     """One sampler call over ``rows`` positions.
 
     logits [rows, V] and E [V, D] are exact fp64 values.  Returns a dict with
@@ -83,15 +122,16 @@ def canvas_sample(logits, E, entropy_bound: float, seed: int, step: int,
         commit |= frozen_m
     else:
         raise ValueError(commit_mode)
+    stored = bf16_round(probs) if probs_storage == "bf16" else probs
     tokens = np.empty(rows, dtype=np.int64)
     for r in range(rows):
         if frozen_m[r]:
             tokens[r] = int(frozen_tokens[r])
         elif commit[r]:
-            tokens[r] = amax[r]
+            tokens[r] = categorical_token(stored[r], key_uniform(renoise_key(seed, step, r))) if categorical \
+                else amax[r]
         else:
             tokens[r] = renoise_token(seed, step, r, V)
-    stored = bf16_round(probs) if probs_storage == "bf16" else probs
     soft = None
     if E is not None:
         E = np.asarray(E, np.float64)

@@ -15,6 +15,9 @@ below is the reading taken:
     token = key mod V
 
 where mix(z) is the output SplitMix64 produces from state z (one ``next``).
+A committed position that takes a categorical draw instead of its argmax
+uses the same key (a position either commits or renoises): its uniform is
+the key's top 24 bits over 2^24, exact in fp32 and fp64.
 """
 from __future__ import annotations
 
@@ -46,3 +49,8 @@ def renoise_key(seed: int, step: int, row: int) -> int:
 
 def renoise_token(seed: int, step: int, row: int, V: int) -> int:
     return renoise_key(seed, step, row) % V
+
+
+def key_uniform(key: int) -> float:
+    """u in [0, 1): the top 24 bits of a 64-bit key over 2^24."""
+    return (key >> 40) / float(1 << 24)

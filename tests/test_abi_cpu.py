@@ -87,3 +87,12 @@ def test_misaligned_buffers_are_rejected_before_any_device_work(cv):
                            good, good, None, None, cv.CANVAS_BF16, good, good, 1 << 30, None)
     assert st == cv.CANVAS_ERR_ARG
     assert "aligned" in cv.canvas_last_error()
+
+
+def test_temperature_schedule_helper_matches_the_oracle(cv):
+    # a host function: no device work
+    from oracle import sampler as osamp
+    for S, hi, lo in ((48, 1.5, 0.25), (12, 1.0, 0.1), (1, 0.7, 0.3), (2, 2.0, 1.0)):
+        for s in range(S):
+            want = osamp.temperature_schedule(s, S, hi, lo)
+            assert abs(cv.canvas_temperature_at(s, S, hi, lo) - want) <= 1e-6 * want

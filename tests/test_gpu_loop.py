@@ -31,6 +31,7 @@ import canvas_workloads as wl
 from canvas_harness import SLACK_EPS, judge_attention
 from oracle import attention as oatt
 from oracle import loop as oloop
+from oracle import sampler as osamp
 from oracle import splitmix
 
 pytestmark = pytest.mark.gpu
@@ -272,3 +273,52 @@ def test_loop_workload_48_steps_invariants(cv):
     committed = _free_run_invariants(cfg, run, cfg.steps)
     assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
     assert committed == 0
+
+
+def test_mini_loop_schedule_categorical_and_adaptive_stop(cv):
+    """The loop with the linear temperature schedule, categorical draws and
+    adaptive stopping: every step follows the sampler's rule at its own
+    temperature (checked against the oracle's sampler on the device's own
+    logits), and the loop stops at the first step where every canvas is
+    committed."""
+    from canvas_denoising_step_03_b300.loop import CanvasLoop
+    cfg = wl.mini_loop_config(steps=24)
+    steps, t_max, t_min = 24, 1.0, 0.05
+    run = CanvasLoop(wl.make_loop_inputs(cfg), schedule=(t_max, t_min, steps), categorical=True)
+    R = cfg.B * cfg.C
+    prev_mask = np.zeros(R, np.uint8)
+    prev_tok = None
+    stopped = None
+    E = wl.as_f64(wl.make_loop_inputs(cfg).E, "bf16")
+    for s in range(steps):
+        run.step()
+        logits = wl.as_f64(np.ascontiguousarray(run.logits.cpu().view(torch.int16).numpy()).view(np.uint16),
+                           "bf16")
+        tau = osamp.temperature_schedule(s, steps, t_max, t_min)
+        assert abs(run.temperature(s) - tau) <= 1e-6 * tau
+        ref = osamp.canvas_sample(logits, E, cfg.bound, cfg.seed, s, temperature=run.temperature(s),
+                                  canvas_len=cfg.C, frozen=prev_mask, frozen_tokens=prev_tok if prev_tok is not None
+                                  else np.zeros(R, np.int64), probs_storage="bf16", categorical=True)
+        mask = run.mask.cpu().numpy()
+        tok = run.tokens.cpu().numpy()
+        ok = np.abs(ref["entropy"] - cfg.bound) > TIE
+        np.testing.assert_array_equal(mask[ok], ref["commit_mask"][ok])
+        # renoised rows take the draw of their own global row
+        ren = np.nonzero((mask == 0) & ok)[0]
+        np.testing.assert_array_equal(tok[ren], [splitmix.renoise_token(cfg.seed, s, int(r), cfg.V) for r in ren])
+        newc = np.nonzero((mask == 1) & (prev_mask == 0) & ok)[0]
+        for r in newc:
+            u = splitmix.key_uniform(splitmix.renoise_key(cfg.seed, s, int(r)))
+            if osamp.categorical_margin(ref["probs"][r], u) > 1e-9:
+                assert tok[r] == osamp.categorical_token(ref["probs"][r], u)
+        counts = run.committed_counts().cpu().numpy()
+        np.testing.assert_array_equal(counts, mask.reshape(cfg.B, cfg.C).sum(axis=1))
+        prev_mask, prev_tok = mask, tok
+        if np.all(osamp.all_committed(mask, cfg.C)):
+            stopped = s + 1
+            break
+    assert stopped is not None, "the schedule should commit every position within the step budget"
+    # the driver's own stopping rule stops at the same step on a fresh run
+    run2 = CanvasLoop(wl.make_loop_inputs(cfg), schedule=(t_max, t_min, steps), categorical=True)
+    assert run2.run(steps) == stopped
+    assert cv.canvas_device_status() == cv.CANVAS_OK

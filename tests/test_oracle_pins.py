@@ -204,7 +204,7 @@ def test_single_key_returns_its_value_row_and_gqa_mapping():
         np.testing.assert_allclose(out[0, 0, h * 16:(h + 1) * 16], v[hk * 16:(hk + 1) * 16], rtol=1e-13)
 
 
-def _sdpa_reference(inp, scale=1.0, v_unit_rms=False, with_lse=False):
+def _sdpa_reference(inp, scale=1.0, v_unit_rms=False, with_lse=False, causal=False):
     """The attention core through torch's scaled_dot_product_attention (fp64)
     with an explicit boolean mask, fed with q/k/v assembled from the pinned
     rms / rotate building blocks; the natural-log softmax normaliser of each
@@ -234,6 +234,9 @@ def _sdpa_reference(inp, scale=1.0, v_unit_rms=False, with_lse=False):
         if c.layer == "sliding" and c.window > 0:
             for i in range(c.C):
                 mask[i, :max(0, P + i - c.window)] = False
+        if causal:   # encode mode: canvas row i sees canvas keys 0..i
+            for i in range(c.C):
+                mask[i, P + i + 1:] = False
         G = c.Hq // c.Hkv
         Kq = np.repeat(K, G, axis=0)
         Vq = np.repeat(Vv, G, axis=0)
@@ -589,3 +592,213 @@ def test_loop_step_row_subset_keeps_global_row_keys():
     np.testing.assert_allclose(sub["entropy"], full["entropy"][sel], rtol=0, atol=0)
     np.testing.assert_allclose(sub["soft_emb"], full["soft_emb"][sel], rtol=1e-15, atol=0)
     assert full["tokens"][1] == 4 and full["tokens"][4] == 7 and full["commit_mask"][[1, 4]].all()
+
+
+# ---------------------------------------------------------------- encode mode and block commit
+@pytest.mark.parametrize("layer,window", [("sliding", 16), ("sliding", 0), ("global", 0)])
+def test_encode_mode_matches_library_sdpa_with_a_causal_mask(layer, window):
+    cfg = _small_cfg(layer=layer, window=window, rotary_fraction=1.0 if layer == "sliding" else 0.25,
+                     gamma_q=None, gamma_k=None, theta=1e6 if layer == "global" else 1e4)
+    inp = wl.make_attention_inputs(cfg)
+    out, _ = _run_oracle(inp, causal=True)
+    np.testing.assert_allclose(out, _sdpa_reference(inp, causal=True), rtol=1e-10, atol=1e-12)
+    # the last canvas row sees the whole block in both modes
+    dec, _ = _run_oracle(inp)
+    np.testing.assert_allclose(out[:, -1], dec[:, -1], rtol=1e-12, atol=1e-14)
+    assert not np.allclose(out[:, 0], dec[:, 0])
+
+
+@pytest.mark.parametrize("layer", ["sliding", "global"])
+def test_encode_row_equals_decode_of_the_truncated_block(layer):
+    # row i of the causal pass = row i of a decode pass over rows 0..i only
+    cfg = _small_cfg(layer=layer, window=16 if layer == "sliding" else 0, C=6,
+                     rotary_fraction=1.0 if layer == "sliding" else 0.25, theta=1e6 if layer == "global" else 1e4)
+    inp = wl.make_attention_inputs(cfg)
+    enc, enc_lse = _run_oracle(inp, causal=True)
+    c = cfg
+    for i in (0, 2, 5):
+        x = _f64(inp, "x")[:, :i + 1]
+        dec, dec_lse = oatt.canvas_attention(x, _f64(inp, "W_q"), _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hq, c.Hkv,
+                                             c.d, inp.gamma_q, inp.gamma_k, c.eps, inp.freq, c.layer,
+                                             _f64(inp, "cache_k"), _f64(inp, "cache_v"), inp.prefix_len, c.window)
+        np.testing.assert_allclose(enc[:, i], dec[:, i], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(enc_lse[:, i], dec_lse[:, i], rtol=1e-12)
+
+
+def _appended_cache(inp, rows_k, rows_v):
+    """Caches [B, Hkv, P+C, d] holding each sequence's prefix then its appended block."""
+    c = inp.cfg
+    B, Hkv, C, d = rows_k.shape
+    P = inp.prefix_len
+    ck = np.full((B, Hkv, int(P.max()) + C, d), np.nan)
+    cv = None if rows_v is None else np.full_like(ck, np.nan)
+    for b in range(B):
+        ck[b, :, :P[b]] = _f64(inp, "cache_k")[b, :, :P[b]]
+        ck[b, :, P[b]:P[b] + C] = rows_k[b]
+        if cv is not None:
+            cv[b, :, :P[b]] = _f64(inp, "cache_v")[b, :, :P[b]]
+            cv[b, :, P[b]:P[b] + C] = rows_v[b]
+    return ck, cv
+
+
+@pytest.mark.parametrize("layer", ["sliding", "global"])
+def test_appended_block_is_what_a_later_token_sees(layer):
+    # commit a block of C rows, then decode one more token over prefix P + C:
+    # the same as decoding a canvas of C + 1 rows (block + token) at its last
+    # row, where the block rows are canvas keys at the same positions
+    cfg = _small_cfg(layer=layer, window=0, C=7, rotary_fraction=1.0 if layer == "sliding" else 0.25,
+                     theta=1e6 if layer == "global" else 1e4)
+    inp = wl.make_attention_inputs(cfg)
+    c = cfg
+    x = _f64(inp, "x")
+    blk, tok = x[:, :-1], x[:, -1:]
+    res = oatt.kv_append(blk, _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hkv, c.d, inp.gamma_k, c.eps, inp.freq, c.layer,
+                         inp.prefix_len, storage="fp64")
+    ck, cv = _appended_cache(inp, res[0], res[1])
+    nxt, _ = oatt.canvas_attention(tok, _f64(inp, "W_q"), _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hq, c.Hkv, c.d,
+                                   inp.gamma_q, inp.gamma_k, c.eps, inp.freq, c.layer, ck, cv,
+                                   inp.prefix_len + blk.shape[1], c.window)
+    full, _ = _run_oracle(inp)
+    np.testing.assert_allclose(nxt[:, 0], full[:, -1], rtol=1e-11, atol=1e-13)
+    # bf16 storage rounds the rows once; the flags mark rounding ties only
+    k16, v16, dk, dv = oatt.kv_append(blk, _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hkv, c.d, inp.gamma_k, c.eps,
+                                      inp.freq, c.layer, inp.prefix_len, storage="bf16", slack_eps=2.0 ** -12)
+    np.testing.assert_array_equal(k16, onum.bf16_round(res[0]))
+    assert np.all((dk == 0) | (np.abs(dk) <= np.abs(k16) * 2.0 ** -7 + 1e-300))
+
+
+@pytest.mark.parametrize("layer", ["sliding", "global"])
+def test_slack_of_tie_rounded_cache_rows_bounds_their_flips(layer):
+    # rows appended with rounding ties: every subset of the alternative
+    # roundings moves the next canvas's output within the slack the oracle
+    # computes from cache_dk / cache_dv
+    cfg = _small_cfg(B=1, C=10, prefix=(60,), D=48, Hq=4, Hkv=2, d=32, window=0, dtype="bf16", gamma_q=2.0,
+                     gamma_k=2.0, seed=17, layer=layer, theta=1e4 if layer == "sliding" else 1e6,
+                     rotary_fraction=1.0 if layer == "sliding" else 0.25)
+    inp = wl.make_attention_inputs(cfg)
+    c = cfg
+    x = _f64(inp, "x")
+    blk, nxt_x = x[:, :6], x[:, 6:]
+    k16, v16, dk, dv = oatt.kv_append(blk, _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hkv, c.d, inp.gamma_k, c.eps,
+                                      inp.freq, c.layer, inp.prefix_len, storage="bf16", slack_eps=2.0 ** -10)
+    assert np.count_nonzero(dk) > 0
+    ck, cv = _appended_cache(inp, k16, v16)
+    dck = np.zeros_like(ck)
+    dck[:, :, 60:66] = dk
+    dcv = None
+    if cv is not None:
+        dcv = np.zeros_like(cv)
+        dcv[:, :, 60:66] = dv
+    args = (nxt_x, _f64(inp, "W_q"), _f64(inp, "W_k"), _f64(inp, "W_v"), c.Hq, c.Hkv, c.d, inp.gamma_q, inp.gamma_k,
+            c.eps, inp.freq, c.layer)
+    P2 = inp.prefix_len + 6
+    ref, _, slack = oatt.canvas_attention(*args, ck, cv, P2, c.window, storage="bf16", slack_eps=2.0 ** -30,
+                                          cache_dk=dck, cache_dv=dcv)
+    ref0, _, slack0 = oatt.canvas_attention(*args, ck, cv, P2, c.window, storage="bf16", slack_eps=2.0 ** -30)
+    assert np.all(slack >= slack0) and np.max(slack - slack0) > 0
+    rng = np.random.default_rng(3)
+    worst = 0.0
+    for _ in range(8):
+        mk = rng.random(dck.shape) < 0.5
+        ck2 = ck + np.where(mk, dck, 0.0)
+        cv2 = None if cv is None else cv + np.where(rng.random(dcv.shape) < 0.5, dcv, 0.0)
+        alt, _ = oatt.canvas_attention(*args, ck2, cv2, P2, c.window, storage="bf16")
+        d = np.abs(alt - ref)
+        assert np.all(d <= slack + 1e-12), float(np.max(d - slack))
+        worst = max(worst, float(d.max()))
+    assert worst > 0
+
+
+# ---------------------------------------------------------------- sampler variants
+def test_temperature_schedule_closed_form():
+    S, hi, lo = 48, 1.5, 0.25
+    ts = [osamp.temperature_schedule(s, S, hi, lo) for s in range(S)]
+    assert ts[0] == hi and ts[-1] == lo
+    assert all(a > b for a, b in zip(ts, ts[1:]))                       # strictly falling
+    np.testing.assert_allclose(np.diff(ts), (lo - hi) / (S - 1), rtol=1e-12)   # equal steps
+    assert osamp.temperature_schedule(0, 1, hi, lo) == hi
+    assert osamp.temperature_schedule(2, 5, 2.0, 1.0) == 1.5             # midpoint by hand
+
+
+def test_categorical_token_is_the_inverse_cdf_by_hand():
+    p = np.array([0.0, 0.125, 0.375, 0.0, 0.5])
+    # boundaries of the cumulative sums: 0.125, 0.5, 1.0
+    assert osamp.categorical_token(p, 0.0) == 1            # the first index with mass
+    assert osamp.categorical_token(p, 0.1249) == 1
+    assert osamp.categorical_token(p, 0.125) == 2          # strict: the boundary moves on
+    assert osamp.categorical_token(p, 0.4999) == 2
+    assert osamp.categorical_token(p, 0.5) == 4            # index 3 has no mass
+    assert osamp.categorical_token(p, 0.9999) == 4
+    # an unnormalised row (stored probabilities) is scaled by its own total
+    assert osamp.categorical_token(2.0 * p, 0.3) == osamp.categorical_token(p, 0.3)
+
+
+def test_categorical_frequencies_follow_the_probabilities():
+    from oracle import splitmix
+    p = np.array([0.05, 0.15, 0.5, 0.3])
+    n = 20000
+    draws = np.array([osamp.categorical_token(p, splitmix.key_uniform(splitmix.renoise_key(9, 2, r)))
+                      for r in range(n)])
+    freq = np.bincount(draws, minlength=4) / n
+    assert np.all(np.abs(freq - p) < 4 * np.sqrt(p * (1 - p) / n))   # within 4 sigma
+
+
+def test_categorical_sampler_changes_only_committed_tokens():
+    from oracle import splitmix
+    rng = np.random.default_rng(4)
+    rows, V = 12, 64
+    logits = rng.standard_normal((rows, V)) * 3.0
+    logits[:6, 5] += 25.0            # peaked rows: commit
+    frozen = np.zeros(rows, np.uint8)
+    frozen[0] = 1
+    ft = np.full(rows, 7)
+    base = osamp.canvas_sample(logits, None, 0.3, 1, 2, frozen=frozen, frozen_tokens=ft, probs_storage="bf16")
+    cat = osamp.canvas_sample(logits, None, 0.3, 1, 2, frozen=frozen, frozen_tokens=ft, probs_storage="bf16",
+                              categorical=True)
+    np.testing.assert_array_equal(cat["commit_mask"], base["commit_mask"])
+    for r in range(rows):
+        if frozen[r] or not base["commit_mask"][r]:
+            assert cat["tokens"][r] == base["tokens"][r]
+        else:
+            u = splitmix.key_uniform(splitmix.renoise_key(1, 2, r))
+            assert cat["tokens"][r] == osamp.categorical_token(cat["probs"][r], u)
+    assert 1 <= int(base["commit_mask"][1:].sum()) < rows - 1
+
+
+def test_all_committed_per_canvas():
+    m = np.array([1, 1, 1, 0, 1, 1, 1, 1], np.uint8)
+    np.testing.assert_array_equal(osamp.all_committed(m, 4), [False, True])
+
+
+# ---------------------------------------------------------------- self-conditioning MLP
+def test_gelu_tanh_form_against_the_exact_gelu_and_its_symmetry():
+    from scipy.special import ndtr
+    x = np.linspace(-8, 8, 4001)
+    g = onum.gelu_tanh(x)
+    # the tanh form approximates x * Phi(x) (Phi: the normal CDF, a library
+    # routine) to within 1e-3 everywhere
+    assert np.max(np.abs(g - x * ndtr(x))) < 1e-3
+    # gelu(x) - gelu(-x) = x exactly (tanh is odd), gelu(0) = 0
+    np.testing.assert_allclose(g - onum.gelu_tanh(-x), x, rtol=1e-13, atol=1e-14)
+    assert onum.gelu_tanh(0.0) == 0.0
+    assert abs(onum.gelu_tanh(20.0) - 20.0) < 1e-12 and abs(onum.gelu_tanh(-20.0)) < 1e-12
+
+
+def test_selfcond_mlp_maps_zero_to_zero_and_is_the_plain_composition():
+    from oracle import loop as oloop
+    rng = np.random.default_rng(5)
+    D, H = 16, 8
+    W1 = onum.bf16_round(rng.standard_normal((H, D)) / 4)
+    W2 = onum.bf16_round(rng.standard_normal((D, H)) / 3)
+    assert np.all(oloop.selfcond_mlp(np.zeros((3, D)), W1, W2) == 0.0)
+    s = rng.standard_normal((5, D))
+    # element by element: row r, output j = sum_k W2[j,k] bf16(gelu(sum_i W1[k,i] bf16(s[r,i])))
+    want = np.zeros((5, D))
+    for r in range(5):
+        for j in range(D):
+            acc = 0.0
+            for k in range(H):
+                h = sum(W1[k, i] * onum.bf16_round(s[r, i]) for i in range(D))
+                acc += W2[j, k] * onum.bf16_round(onum.gelu_tanh(h))
+            want[r, j] = acc
+    np.testing.assert_allclose(oloop.selfcond_mlp(s, W1, W2), want, rtol=1e-12, atol=1e-14)
