@@ -11,6 +11,7 @@ trained weights are involved.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --workload loop --prefix P [--steps K] [--warmup W]
     python bench.py --workload sliding [--steps K] [--warmup W]
+    python bench.py --workload moe [--steps K] [--warmup W]
 
 Prints ONE JSON line (rank 0).  ``--workload loop`` times instead the batched
 denoising loop (4 canvases x 256, 5 sliding + 1 global layers, vocab 262144,
@@ -527,6 +528,110 @@ def run_sliding(args, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------------------------- mixture of experts
+MOE_WORKLOAD = ("mixture-of-experts block: canvas_moe R=1024 tokens (4 canvases x 256) D=2816, 128 experts "
+                "(top-8) of width 704 + 1 shared expert of width 704, gated GELU, random bf16 weights")
+
+
+def run_moe(args, rank, world, local_rank):
+    """canvas_moe on R = 1024 tokens with the pages' routing shape (128 experts,
+    8 active + 1 shared): calls/s, the GEMM rate, and weight streaming against
+    HBM (each expert's weights are read once per call for the few dozen tokens
+    routed to it, so the call is bound by memory, not the tensor cores)."""
+    import torch
+    import torch.distributed as dist
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import canvas_denoising_step_03_b300 as cv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    R, D, E, F, k, Fs = 1024, 2816, 128, 704, 8, 704
+    gen = torch.Generator(device=dev).manual_seed(17)
+
+    def w(*shape, std):
+        return (torch.randn(*shape, device=dev, generator=gen) * std).to(torch.bfloat16)
+
+    x = w(R, D, std=1.0)
+    router = w(E, D, std=D ** -0.5)
+    Wg, Wu = w(E * F, D, std=D ** -0.5), w(E * F, D, std=D ** -0.5)
+    Wd = w(E * D, F, std=F ** -0.5)
+    Sg, Su, Sd = w(Fs, D, std=D ** -0.5), w(Fs, D, std=D ** -0.5), w(D, Fs, std=Fs ** -0.5)
+    out = torch.empty((R, D), device=dev)
+    ws = cv.workspace(cv.canvas_moe_workspace_size(R, D, E, F, k, Fs), dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(xin):
+        cv.canvas_moe(xin, router, k, None, Wg, Wu, Wd, Sg, Su, Sd, out, None, None, ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call(x)
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = cv.canvas_kernel_launches()
+    for e0, e1 in evs:
+        flush.fill_(1.0)
+        e0.record(stream)
+        call(x)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    launches = cv.canvas_kernel_launches() - launches0
+    clk = clocks.stop()
+    assert cv.canvas_device_status() == cv.CANVAS_OK, cv.canvas_last_error()
+    ms = max_over_ranks([statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)], dev)[0]
+    # end to end: tokens from pinned host memory in, the block's output out
+    x_h = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+    x_h.copy_(x.cpu())
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    e2e = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        call(x_d)
+        out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        if i >= args.warmup:
+            e2e.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks([statistics.median(e0.elapsed_time(e1) for e0, e1 in e2e)], dev)[0]
+    if rank != 0:
+        return None
+    hbm, bf16, peak_src = measured_peaks()
+    flops = 2.0 * R * D * E + 3 * 2.0 * R * k * D * F + 3 * 2.0 * R * D * Fs
+    wbytes = 2.0 * (E * D + 3 * E * F * D + 3 * Fs * D)
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": round(world * 1000.0 / ms, 3), "unit": "moe block calls/s (1024 tokens)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random weights and tokens; no dataset)",
+        "config": {"workload": MOE_WORKLOAD, "l2": "flushed between timed calls (252 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "roofline": {"kernel": "canvas_moe call (router, grouped expert GEMMs, shared expert)", "bound": "hbm",
+                     "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "traffic": None, "algorithmic": f"{wbytes:.4g} B of weights per call, each read once",
+                     "peak_source": f"{peak_src}"},
+        "e2e": {"value": round(world * 1000.0 / e2e_ms, 3), "unit": "moe block calls/s (1024 tokens)",
+                "h2d_bytes_per_step": int(x_h.numel() * 2), "d2h_bytes_per_step": int(out_h.numel() * 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
+
+
 # --------------------------------------------------------------------------- the batched loop
 def run_loop(args, rank, world, local_rank):
     """Steps of the batched denoising loop (canvas_denoising_step_03_b300.loop):
@@ -771,7 +876,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="step", choices=["step", "loop", "sliding"])
+    ap.add_argument("--workload", default="step", choices=["step", "loop", "sliding", "moe"])
     ap.add_argument("--prefix", type=int, default=1024, help="committed prefix of the loop workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
@@ -788,6 +893,8 @@ def main():
         line = run_loop(args, rank, world, local_rank)
     elif args.workload == "sliding":
         line = run_sliding(args, rank, world, local_rank)
+    elif args.workload == "moe":
+        line = run_moe(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0 and line is not None:

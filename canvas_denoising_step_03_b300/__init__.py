@@ -40,7 +40,7 @@ EXPORTED = [
     "canvas_version", "canvas_profile_events", "canvas_kernel_launches", "canvas_gemm_bf16_noalloc",
     "canvas_embed_input", "canvas_cast_bf16", "canvas_gemm_bf16_to_bf16", "canvas_selftest_wait_timeout",
     "canvas_attention_encode", "canvas_kv_append_workspace_size", "canvas_kv_append", "canvas_count_committed",
-    "canvas_temperature_at", "canvas_gelu_bf16",
+    "canvas_temperature_at", "canvas_gelu_bf16", "canvas_moe_workspace_size", "canvas_moe",
 ]
 
 # size of the static scratch behind canvas_gemm_bf16_noalloc (include/canvas.h)
@@ -82,6 +82,10 @@ def _load(path: str = LIB_PATH):
     lib.canvas_kv_append.argtypes = [P, I, I, I, I, P, P, I, I, P, F, P, I, ctypes.POINTER(canvas_kv_cache), P, I,
                                      P, Z, P]
     lib.canvas_kv_append.restype = I
+    lib.canvas_moe_workspace_size.argtypes = [I] * 6
+    lib.canvas_moe_workspace_size.restype = Z
+    lib.canvas_moe.argtypes = [P, I, I, P, I, I, P, P, P, P, I, P, P, P, I, P, P, P, P, Z, P]
+    lib.canvas_moe.restype = I
     lib.canvas_gelu_bf16.argtypes = [P, P, Z, P]
     lib.canvas_gelu_bf16.restype = I
     lib.canvas_count_committed.argtypes = [P, I, I, P, P]
@@ -242,6 +246,24 @@ def canvas_sample(logits, E, entropy_bound, seed, step, temperature, commit_mode
                              _ptr(entropy), _ptr(confidence), _ptr(argmax), _ptr(probs_out), int(probs_dtype),
                              _ptr(soft_emb), _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def canvas_moe_workspace_size(R, D, E, F, k, Fs) -> int:
+    return lib.canvas_moe_workspace_size(int(R), int(D), int(E), int(F), int(k), int(Fs))
+
+
+def canvas_moe(x, router, k, expert_scale, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, out, topk_idx, topk_w,
+               workspace, stream=None):
+    """Mixture-of-experts block: x [R, D] bf16, router [E, D], W_gate / W_up
+    [E*F, D], W_down [E*D, F], shared expert Ws_* (or None), out [R, D] fp32."""
+    R, D = x.shape
+    E = router.shape[0]
+    F = W_gate.shape[0] // E
+    Fs = 0 if Ws_gate is None else Ws_gate.shape[0]
+    _check(lib.canvas_moe(_ptr(x), R, D, _ptr(router), E, int(k), _ptr(expert_scale), _ptr(W_gate), _ptr(W_up),
+                          _ptr(W_down), F, _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), Fs, _ptr(out), _ptr(topk_idx),
+                          _ptr(topk_w), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(stream)))
 
 
 def canvas_gelu_bf16(inp, out, stream=None):

@@ -235,6 +235,8 @@ canvas_status run_gemm_group(const void* A, const void* const* B, void* const* C
   g.b_mn_major = b_mn_major;
   g.two_acc = p.two_acc;
   g.m_tiles = p.m_tiles;
+  g.bm = 256;
+  g.group_of_mtile = nullptr;
   g.nprob = nprob;
   // partials_out: the caller sums a split product's partials itself
   const bool reduce = partials_out == nullptr;
@@ -250,6 +252,55 @@ canvas_status run_gemm_tc(const void* A, const void* B, int b_mn_major, float* C
                           int accumulate, void* ws, cudaStream_t stream) {
   void* Cv = C;
   return run_gemm_group(A, &B, &Cv, &N, 1, b_mn_major, M, K, accumulate, 0, ws, stream);
+}
+
+// Grouped products: C_p[Mpad, N_p] = A[Mpad, K] B_p[group(tile), N_p rows, K]^T
+// for nprob problems sharing A, every 128-row tile of A in one group
+// (group_of_mtile, device; -1: no work), B_p stored as [groups * N_p, K].
+// One launch, no K split; C fp32, or bf16 with out_bf16.
+canvas_status run_gemm_grouped(const void* A, const void* const* B, void* const* C, const int* N, int nprob,
+                               int groups, const int* group_of_mtile, int Mpad, int K, int out_bf16,
+                               cudaStream_t stream) {
+  if (nprob < 1 || nprob > kGemmMaxProblems || Mpad % 128 != 0)
+    return fail(CANVAS_ERR_ARG, "grouped GEMM: 1 to 3 problems, rows in whole 128-row tiles");
+  GemmTcMaps maps;
+  GemmTcArgs g;
+  canvas_status st = make_map_bf16(&maps.A, A, Mpad, K, kGemmBM, kGemmBK);
+  if (st != CANVAS_OK) return st;
+  g.tile0[0] = 0;
+  for (int i = 0; i < nprob; ++i) {
+    st = make_map_bf16(&maps.B[i], B[i], uint64_t(groups) * N[i], K, kGemmBN, kGemmBK);
+    if (st != CANVAS_OK) return st;
+    st = out_bf16 ? make_map_bf16_store(&maps.out[i], C[i], 1, uint64_t(Mpad), uint64_t(N[i]), uint64_t(N[i]))
+                  : make_map_f32_store(&maps.out[i], C[i], 1, uint64_t(Mpad), uint64_t(N[i]), uint64_t(N[i]));
+    if (st != CANVAS_OK) return st;
+    g.C[i] = C[i];
+    g.N[i] = N[i];
+    g.partials[i] = nullptr;
+    g.tile0[i + 1] = g.tile0[i] + (N[i] + kGemmBN - 1) / kGemmBN;
+  }
+  for (int i = nprob; i < kGemmMaxProblems; ++i) {
+    maps.B[i] = maps.B[0];
+    maps.out[i] = maps.out[0];
+    g.C[i] = nullptr;
+    g.partials[i] = nullptr;
+    g.N[i] = 0;
+    g.tile0[i + 1] = g.tile0[i];
+  }
+  g.M = Mpad;
+  g.K = K;
+  g.kblocks = (K + kGemmBK - 1) / kGemmBK;
+  g.splits = 1;
+  g.accumulate = 0;
+  g.out_bf16 = out_bf16;
+  g.b_mn_major = 0;
+  g.two_acc = 0;
+  g.m_tiles = Mpad / 128;
+  g.bm = 128;
+  g.group_of_mtile = group_of_mtile;
+  g.nprob = nprob;
+  CANVAS_CUDA(launch_gemm_tc(maps, g, stream));
+  return CANVAS_OK;
 }
 
 // ------------------------------------------------------------------ attention layout
@@ -850,6 +901,142 @@ canvas_status canvas_kv_append(const void* x, int dtype, int B, int C, int D, co
   p.eps = eps;
   p.global = global ? 1 : 0;
   CANVAS_CUDA(launch_kv_append(p, bf16, stream));
+  return CANVAS_OK;
+}
+
+// ------------------------------------------------------------------ mixture of experts
+struct MoeLayout {
+  size_t scores, topk_idx, topk_w, counts, offsets, cursor, tiles, slot, xg, hg, hu, ag, yg, hs_g, hs_u, as, ys,
+      gemm, total;
+  int max_tiles;
+};
+
+static MoeLayout moe_layout(int R, int D, int E, int F, int k, int Fs) {
+  MoeLayout L;
+  // every expert's rows padded to whole 128-row tiles: at most R k + E 127 rows
+  L.max_tiles = int((size_t(R) * k + size_t(E) * 127 + 127) / 128);
+  const size_t Mpad = size_t(L.max_tiles) * 128;
+  L.scores = size_t(R) * E * 4;
+  L.topk_idx = size_t(R) * k * 4;
+  L.topk_w = size_t(R) * k * 4;
+  L.counts = size_t(E) * 4;
+  L.offsets = size_t(E + 1) * 4;
+  L.cursor = size_t(E) * 4;
+  L.tiles = size_t(L.max_tiles) * 4;
+  L.slot = size_t(R) * k * 4;
+  L.xg = Mpad * D * 2;
+  L.hg = Mpad * F * 4;
+  L.hu = L.hg;
+  L.ag = Mpad * F * 2;
+  L.yg = Mpad * D * 4;
+  L.hs_g = Fs > 0 ? size_t(R) * Fs * 4 : 0;
+  L.hs_u = L.hs_g;
+  L.as = Fs > 0 ? size_t(R) * Fs * 2 : 0;
+  L.ys = Fs > 0 ? size_t(R) * D * 4 : 0;
+  size_t g = gemm_ws_bytes(plan_gemm(R, E, D));
+  if (Fs > 0) {
+    const int Ns[2] = {Fs, Fs};
+    g = std::max(g, gemm_ws_bytes(plan_gemm_group(R, Ns, 2, D)));
+    g = std::max(g, gemm_ws_bytes(plan_gemm(R, D, Fs)));
+  }
+  L.gemm = g;
+  L.total = align_up(L.scores) + align_up(L.topk_idx) + align_up(L.topk_w) + align_up(L.counts) +
+            align_up(L.offsets) + align_up(L.cursor) + align_up(L.tiles) + align_up(L.slot) + align_up(L.xg) +
+            align_up(L.hg) + align_up(L.hu) + align_up(L.ag) + align_up(L.yg) + align_up(L.hs_g) +
+            align_up(L.hs_u) + align_up(L.as) + align_up(L.ys) + align_up(L.gemm) + kAlign;
+  return L;
+}
+
+static bool moe_shape_ok(int R, int D, int E, int F, int k, int Fs) {
+  return R >= 1 && D >= 8 && D % 8 == 0 && E >= 1 && E <= 256 && F >= 8 && F % 8 == 0 && k >= 1 && k <= 16 &&
+         k <= E && Fs >= 0 && Fs % 8 == 0 && E % 8 == 0;
+}
+
+size_t canvas_moe_workspace_size(int R, int D, int E, int F, int k, int Fs) {
+  if (!moe_shape_ok(R, D, E, F, k, Fs)) return 0;
+  return moe_layout(R, D, E, F, k, Fs).total;
+}
+
+canvas_status canvas_moe(const void* x, int R, int D, const void* router, int E, int k, const float* expert_scale,
+                         const void* W_gate, const void* W_up, const void* W_down, int F, const void* Ws_gate,
+                         const void* Ws_up, const void* Ws_down, int Fs, float* out, int32_t* topk_idx,
+                         float* topk_w, void* workspace, size_t ws_bytes, canvas_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!moe_shape_ok(R, D, E, F, k, Fs))
+    return fail(CANVAS_ERR_ARG, "canvas_moe: shape (D, F, Fs multiples of 8; E a multiple of 8 up to 256; 1 <= k <= 16, k <= E)");
+  if (!x || !router || !W_gate || !W_up || !W_down || !out) return fail(CANVAS_ERR_ARG, "canvas_moe: null pointer");
+  if (Fs > 0 && (!Ws_gate || !Ws_up || !Ws_down)) return fail(CANVAS_ERR_ARG, "canvas_moe: shared expert weights");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(CANVAS_ERR_ARG, "canvas_moe: x and out must be 16-byte aligned");
+  const MoeLayout L = moe_layout(R, D, E, F, k, Fs);
+  if (!ws_ok(workspace, ws_bytes, L.total))
+    return fail(CANVAS_ERR_WORKSPACE, "canvas_moe: workspace missing, small or misaligned (need %zu)", L.total);
+  Carver cv(workspace);
+  MoeArgs a;
+  a.R = R;
+  a.D = D;
+  a.E = E;
+  a.k = k;
+  a.max_tiles = L.max_tiles;
+  float* scores = cv.take<float>(L.scores);
+  a.scores = scores;
+  a.expert_scale = expert_scale;
+  int32_t* idx_ws = cv.take<int32_t>(L.topk_idx);
+  float* w_ws = cv.take<float>(L.topk_w);
+  a.topk_idx = topk_idx ? topk_idx : idx_ws;
+  a.topk_w = topk_w ? topk_w : w_ws;
+  a.counts = cv.take<int32_t>(L.counts);
+  a.offsets = cv.take<int32_t>(L.offsets);
+  a.cursor = cv.take<int32_t>(L.cursor);
+  a.group_of_mtile = cv.take<int32_t>(L.tiles);
+  a.slot = cv.take<int32_t>(L.slot);
+  a.x = x;
+  a.xg = cv.take<char>(L.xg);
+  float* hg = cv.take<float>(L.hg);
+  float* hu = cv.take<float>(L.hu);
+  void* ag = cv.take<char>(L.ag);
+  float* yg = cv.take<float>(L.yg);
+  float* hs_g = cv.take<float>(L.hs_g);
+  float* hs_u = cv.take<float>(L.hs_u);
+  void* as = cv.take<char>(L.as);
+  float* ys = cv.take<float>(L.ys);
+  void* gws = cv.take<char>(L.gemm);
+  a.yg = yg;
+  a.ys = Fs > 0 ? ys : nullptr;
+  a.out = out;
+  const int Mpad = L.max_tiles * 128;
+  // 1. router scores, top-k, weights, grouped rows
+  canvas_status st = run_gemm_tc(x, router, 0, scores, R, E, D, 0, gws, stream);
+  if (st != CANVAS_OK) return st;
+  CANVAS_CUDA(launch_moe_route(a, stream));
+  // 2. the routed experts: gate and up in one grouped launch, the gated
+  //    activation, down
+  {
+    const void* Bs[2] = {W_gate, W_up};
+    void* Cs[2] = {hg, hu};
+    const int Ns[2] = {F, F};
+    st = run_gemm_grouped(a.xg, Bs, Cs, Ns, 2, E, a.group_of_mtile, Mpad, D, 0, stream);
+    if (st != CANVAS_OK) return st;
+    CANVAS_CUDA(launch_moe_act(hg, hu, ag, (long long)Mpad * F, stream));
+    const void* Bd[1] = {W_down};
+    void* Cd[1] = {yg};
+    const int Nd[1] = {D};
+    st = run_gemm_grouped(ag, Bd, Cd, Nd, 1, E, a.group_of_mtile, Mpad, F, 0, stream);
+    if (st != CANVAS_OK) return st;
+  }
+  // 3. the shared expert on every token
+  if (Fs > 0) {
+    const void* Bs[2] = {Ws_gate, Ws_up};
+    void* Cs[2] = {hs_g, hs_u};
+    const int Ns[2] = {Fs, Fs};
+    st = run_gemm_group(x, Bs, Cs, Ns, 2, 0, R, D, 0, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+    CANVAS_CUDA(launch_moe_act(hs_g, hs_u, as, (long long)R * Fs, stream));
+    st = run_gemm_tc(as, Ws_down, 0, ys, R, D, Fs, 0, gws, stream);
+    if (st != CANVAS_OK) return st;
+  }
+  // 4. out = sum of weighted expert outputs + shared
+  CANVAS_CUDA(launch_moe_combine(a, stream));
   return CANVAS_OK;
 }
 

@@ -62,6 +62,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.y, split = blockIdx.z;
+  // grouped mode: this tile's group selects the B rows (uniform over the CTA,
+  // decided before any barrier or TMEM allocation)
+  int group = 0;
+  if (g.group_of_mtile != nullptr) {
+    group = g.group_of_mtile[mt];
+    if (group < 0) return;
+  }
   // problem of this tile (selects, not indexed loads, so the arguments stay in constant memory)
   const int prob = (g.nprob > 1 && int(blockIdx.x) >= g.tile0[1]) + (g.nprob > 2 && int(blockIdx.x) >= g.tile0[2]);
   const int nt = int(blockIdx.x) - (prob == 0 ? 0 : prob == 1 ? g.tile0[1] : g.tile0[2]);
@@ -74,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = split * kb_per + min(split, kb_rem);
   const int nkb = kb_per + (split < kb_rem ? 1 : 0);
   const int nacc = g.two_acc ? 2 : 1;
+  const int brow0 = group * N;  // first B row of this tile's group (0 unless grouped)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
@@ -109,11 +117,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kx = (kb0 + i) * kGemmBK;
         mbar_arrive_expect_tx(&full[s], bytes);
         uint8_t* a = sA + s * kAStageBytes;
-        tma_load_2d(a, tmA, &full[s], kx, mt * 256);
-        if (nacc == 2) tma_load_2d(a + kABoxBytes, tmA, &full[s], kx, mt * 256 + 128);
+        tma_load_2d(a, tmA, &full[s], kx, mt * g.bm);
+        if (nacc == 2) tma_load_2d(a + kABoxBytes, tmA, &full[s], kx, mt * g.bm + 128);
         uint8_t* b = sB + s * kBStageBytes;
         if (!g.b_mn_major) {
-          tma_load_2d(b, tmB, &full[s], kx, nt * kGemmBN);
+          tma_load_2d(b, tmB, &full[s], kx, brow0 + nt * kGemmBN);
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tma_load_2d(b + c * 8192, tmB, &full[s], nt * kGemmBN + 64 * c, kx);
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int step = pack ? 2 : 1;  // 32-column TMEM chunks per box
       int nbox = 0;
       for (int acc = 0; acc < nacc; ++acc) {
-        const int row0 = mt * 256 + acc * 128 + q * 32;
+        const int row0 = mt * g.bm + acc * 128 + q * 32;
         if (row0 >= g.M) break;  // uniform in the warp
         for (int cc = 0; cc < kGemmBN / 32; cc += step) {
           const int col0 = nt * kGemmBN + cc * 32;
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok) {
       // C += A op(B) with a single split: read-modify-write of whole rows
       for (int acc = 0; acc < nacc; ++acc) {
-        const int row = mt * 256 + acc * 128 + q * 32 + lane;
+        const int row = mt * g.bm + acc * 128 + q * 32 + lane;
         for (int cc = 0; cc < kGemmBN / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(tmem + uint32_t(acc * 256 + cc * 32) + (uint32_t(q * 32) << 16), r);

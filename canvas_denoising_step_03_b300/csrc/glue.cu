@@ -66,9 +66,11 @@ __global__ void __launch_bounds__(256) cast_bf16_kernel(const float4* __restrict
   }
 }
 
-// out = bf16(gelu(in)), GELU in its tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x +
-// 0.044715 x^3))) evaluated in fp32 (tanhf), rounded once: the activation of
-// the self-conditioning MLP.
+// out = bf16(gelu(in)), GELU in its tanh form 0.5 x (1 + tanh(u)), u =
+// sqrt(2/pi) (x + 0.044715 x^3), rounded once: the activation of the
+// self-conditioning MLP.  Evaluated as x / (1 + exp(-2u)) (the identity
+// 1 + tanh(u) = 2 / (1 + exp(-2u))), which keeps its relative accuracy for
+// negative x, where 1 + tanh(u) would cancel.
 __global__ void __launch_bounds__(256) gelu_bf16_kernel(const float4* __restrict__ in, uint4* __restrict__ out,
                                                         long long n8) {
   const float k0 = 0.7978845608028654f, k1 = 0.044715f;
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(256) gelu_bf16_kernel(const float4* __restrict
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float x = v[j];
-      v[j] = 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+      v[j] = x / (1.0f + expf(-2.0f * k0 * (x + k1 * x * x * x)));
     }
     out[e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                         pack_bf16x2(v[6], v[7]));

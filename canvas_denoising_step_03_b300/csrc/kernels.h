@@ -13,6 +13,8 @@ namespace canvas {
 void count_launches(int n);
 
 // ----------------------------------------------------------------- sampler
+// a row's CTAs: up to 8, each staging up to a 64 KB slice of the row (16 CTAs
+// with 32 KB slices measured slower: 75.8 against 63.5 us on 256 x 262144)
 constexpr int kMaxSampleCluster = 8;
 
 struct SampleArgs {
@@ -45,6 +47,11 @@ struct GemmTcArgs {
   int b_mn_major;  // 0: B is [N,K] (K contiguous); 1: B is [K,N] (N contiguous)
   int two_acc;     // 1: a CTA covers 256 rows (two 128-row accumulators)
   int m_tiles, nprob;
+  int bm;                    // rows per M tile: 256 (two accumulators when M > 128) or 128 (grouped)
+  // grouped mode (non-null): M tile t belongs to group group_of_mtile[t] (-1:
+  // no work), whose B rows are group * N_p .. of a [groups * N_p, K] B; the
+  // rows of A are laid out so that no tile straddles two groups
+  const int* group_of_mtile;
   int tile0[kGemmMaxProblems + 1];  // first 256-column tile of each problem; tile0[nprob] = all tiles
   int N[kGemmMaxProblems];
   void* C[kGemmMaxProblems];
@@ -197,6 +204,28 @@ struct AttnTcMaps {
 size_t attention_tc_smem_bytes(int d);
 cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream);
 cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream);
+
+// ----------------------------------------------------------------- mixture of experts
+struct MoeArgs {
+  int R, D, E, k, max_tiles;
+  const float* scores;         // [R, E] router scores x . router_e
+  const float* expert_scale;   // [E] or null (1)
+  int32_t* topk_idx;           // [R, k] chosen experts, largest score first
+  float* topk_w;               // [R, k] their weights
+  int32_t* counts;             // [E] tokens per expert
+  int32_t* offsets;            // [E + 1] first row of each expert in the grouped layout
+  int32_t* cursor;             // [E] fill positions
+  int32_t* group_of_mtile;     // [max_tiles] expert of each 128-row tile, -1 past the end
+  int32_t* slot;               // [R, k] row of each (token, choice) in the grouped layout
+  const void* x;               // [R, D] bf16 input
+  void* xg;                    // [max_tiles * 128, D] bf16 rows grouped by expert
+  const float* yg;             // [max_tiles * 128, D] expert outputs (grouped rows)
+  const float* ys;             // [R, D] shared expert output or null
+  float* out;                  // [R, D]
+};
+cudaError_t launch_moe_route(const MoeArgs& a, cudaStream_t stream);  // route, offsets, scatter
+cudaError_t launch_moe_act(const float* gate, const float* up, void* act, long long n, cudaStream_t stream);
+cudaError_t launch_moe_combine(const MoeArgs& a, cudaStream_t stream);
 
 // ----------------------------------------------------------------- loop glue
 cudaError_t launch_embed_input(const int32_t* tokens, const void* E, const float* soft, int rows, int D, int V,

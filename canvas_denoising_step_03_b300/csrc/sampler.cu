@@ -218,7 +218,7 @@ __device__ __forceinline__ RowState reduce_row(RowState s, RowState* warp_part, 
 // needs no cluster-wide barrier; one cluster barrier, split into an arrive
 // after the exchange and a wait before exit, keeps every CTA alive until all
 // stores into it have landed.
-constexpr int kSmemSliceBytes = 65536;
+constexpr int kSmemSliceBytes = 65536;   // largest staged slice
 constexpr int kPieceElems = 8192;
 constexpr int kMaxPieces = kSmemSliceBytes / (2 * kPieceElems);
 
@@ -237,12 +237,13 @@ __device__ __forceinline__ float bf16x2_max(uint32_t a, uint32_t b, uint32_t c, 
 // about that exact maximum -- no running rescale, no data-dependent branch
 // per group.  Thread t owns 16-byte chunks t + kThreads k of the slice (8
 // logits each, increasing with k), read conflict-free from shared memory.
-// kFull: the slice is exactly kSmemSliceBytes (compile-time trip counts).
-template <int kThreads, bool kFull>
+// kSlice: the staged slice's bytes (at most kSmemSliceBytes); kFull: every
+// slice is exactly that long (compile-time trip counts).
+template <int kThreads, int kSlice, bool kFull>
 __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a,
                                                                      const __nv_bfloat16* __restrict__ logits) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kMaxK = kSmemSliceBytes / 16 / kThreads;           // chunks per thread
+  constexpr int kMaxK = kSlice / 16 / kThreads;                    // chunks per thread
   constexpr int kKPerPiece = kPieceElems / 8 / kThreads;            // of them in one bulk-copy piece
   static_assert(kKPerPiece >= 1 && kMaxK % kKPerPiece == 0, "piece layout");
   extern __shared__ __align__(128) uint8_t slice_raw[];
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
   const uint32_t csize = gridDim.x;
   const long long c0 = (long long)rank * a.chunk;
   const long long c1 = min((long long)a.V, c0 + a.chunk);
-  const int n = kFull ? kSmemSliceBytes / 2 : (c1 > c0 ? int(c1 - c0) : 0);  // a multiple of 8
+  const int n = kFull ? kSlice / 2 : (c1 > c0 ? int(c1 - c0) : 0);  // a multiple of 8
   const int nch = n / 8;
   const __nv_bfloat16* src = logits + (long long)row * a.V + c0;
   const uint4* slice4 = reinterpret_cast<const uint4*>(slice_raw);
@@ -585,19 +586,21 @@ cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, c
   if (bf16 && size_t(a.chunk) * 2 <= size_t(kSmemSliceBytes)) {
     static bool attr_set = false;
     if (!attr_set) {
-      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemSliceBytes);
+      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, kSmemSliceBytes, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemSliceBytes);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemSliceBytes);
+      e = cudaFuncSetAttribute(sample_rows_smem_kernel<kThreads, kSmemSliceBytes, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemSliceBytes);
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
     cfg.dynamicSmemBytes = size_t(a.chunk) * 2;
     // every CTA's slice exactly full: compile-time trip counts
-    const bool full = size_t(a.chunk) * 2 == size_t(kSmemSliceBytes) && (long long)a.chunk * a.cluster == a.V;
-    e = full ? cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, true>, a, lb)
-             : cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, false>, a, lb);
+    const bool whole = (long long)a.chunk * a.cluster == a.V;
+    if (whole && size_t(a.chunk) * 2 == size_t(kSmemSliceBytes))
+      e = cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, kSmemSliceBytes, true>, a, lb);
+    else
+      e = cudaLaunchKernelEx(&cfg, sample_rows_smem_kernel<kThreads, kSmemSliceBytes, false>, a, lb);
   } else if (bf16) {
     e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<__nv_bfloat16, kThreads>, a, lb);
   } else {

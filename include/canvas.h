@@ -331,8 +331,10 @@ canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stre
 
 /*
  * canvas_gelu_bf16 -- out[i] = bf16(gelu(in[i])), GELU in its tanh form
- * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated in fp32 and
- * rounded once (nearest even); n % 8 == 0, both 16-byte aligned.  Glue: the
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated in fp32 as
+ * x / (1 + exp(-2 sqrt(2/pi) (x + 0.044715 x^3))) (the same function, with
+ * no cancellation for negative x) and rounded once (nearest even);
+ * n % 8 == 0, both 16-byte aligned.  Glue: the
  * activation of the self-conditioning MLP ([AIT] glossary, self-conditioning:
  * the expected embedding P.E passes through a small MLP that maps zero to
  * zero before it is added to the canvas input), built as
@@ -340,6 +342,43 @@ canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stre
  *   canvas_gemm_bf16, canvas_gelu_bf16, canvas_gemm_bf16; no biases).
  */
 canvas_status canvas_gelu_bf16(const float* in, void* out, size_t n, canvas_stream_t stream);
+
+/* Workspace (bytes) that canvas_moe needs; 0 for an invalid shape. */
+size_t canvas_moe_workspace_size(int R, int D, int E, int F, int k, int Fs);
+
+/*
+ * canvas_moe -- a mixture-of-experts MLP block on R tokens.
+ *
+ * Defined by [AIT] glossary "혼합 전문가(MoE)" (each token goes to its top-k
+ * experts, which run in parallel and are summed with weights, plus a shared
+ * expert every token passes through; the routing score is the exponential of
+ * the router key's dot product with the input, renormalised and scaled) and
+ * [TC] "아키텍처" (128 experts, 8 active + 1 shared).  The pages print no
+ * expert MLP; the Gemma family's gated form is taken:
+ *   s_e   = x . router_e                         (fp32 accumulation)
+ *   top-k by s (equal scores: lower expert index first)
+ *   w_j   = exp(s_j - s_max) / sum_{chosen} exp(s_i - s_max) * scale_e
+ *   y_e   = W_down_e bf16(gelu(W_gate_e x) * (W_up_e x))   (GELU tanh form)
+ *   out   = sum_j w_j y_{e_j}  (in choice order)  +  y_shared(x)
+ *
+ *   x        [R, D] bf16, 16-byte aligned
+ *   router   [E, D] bf16 router keys
+ *   expert_scale [E] fp32 or NULL (all 1)
+ *   W_gate, W_up [E * F, D] bf16 (expert e: rows e*F ..), W_down [E * D, F] bf16
+ *   Ws_gate, Ws_up [Fs, D], Ws_down [D, Fs] bf16: the shared expert (Fs = 0: none)
+ *   out      [R, D] fp32 out, 16-byte aligned
+ *   topk_idx [R, k] int32, topk_w [R, k] fp32: out, or NULL
+ *   workspace, ws_bytes  >= canvas_moe_workspace_size(R, D, E, F, k, Fs)
+ * Requires D, F, Fs multiples of 8, E a multiple of 8 up to 256, 1 <= k <= 16,
+ * k <= E.  The experts run as grouped tensor-core GEMMs over the tokens
+ * routed to them (each expert's rows padded to whole 128-row tiles).
+ * Asynchronous on `stream`.
+ */
+canvas_status canvas_moe(const void* x, int R, int D, const void* router, int E, int k, const float* expert_scale,
+                         const void* W_gate, const void* W_up, const void* W_down, int F,
+                         const void* Ws_gate, const void* Ws_up, const void* Ws_down, int Fs,
+                         float* out, int32_t* topk_idx, float* topk_w,
+                         void* workspace, size_t ws_bytes, canvas_stream_t stream);
 
 /*
  * canvas_count_committed -- committed positions of each canvas, for adaptive

@@ -28,9 +28,10 @@ every function cites the page and the section it follows:
 Modules: ``numerics`` (rms, rotate, RoPE spectrum, bf16 rounding),
 ``attention`` (the canvas attention layer), ``sampler`` (softmax, entropy,
 argmax, commit/renoise, soft embedding), ``splitmix`` (the counter RNG),
-``loop`` (one step of the multi-layer denoising loop).
+``loop`` (one step of the multi-layer denoising loop, the self-conditioning
+MLP), ``moe`` (a mixture-of-experts MLP block).
 
 Parity status: every function is pinned by the CPU tests in
 ``tests/test_oracle_pins.py`` except where a docstring says "parity unpinned".
 """
-from . import numerics, attention, sampler, splitmix, loop  # noqa: F401
+from . import numerics, attention, sampler, splitmix, loop, moe  # noqa: F401

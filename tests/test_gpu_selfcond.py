@@ -33,6 +33,15 @@ def spacing(a):
     return np.ldexp(1.0, (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7).astype(int))
 
 
+def gelu_rel_err(x):
+    """Relative error of the device's fp32 GELU, x / (1 + exp(-2u)): a few
+    units of 2^-24 from the division and exp, plus the argument's own
+    rounding (about 3 units of 2^-24 of |2u|) magnified by exp's condition
+    number |2u| where exp(-2u) dominates."""
+    u2 = 2.0 * np.sqrt(2.0 / np.pi) * np.abs(x + 0.044715 * x ** 3)
+    return (3.0 * u2 + 8.0) * 2.0 ** -24
+
+
 def tie_mask(y, rel):
     """Where bf16 rounding of y is ambiguous within a relative error ``rel``."""
     s = onum.bf16_round(y)
@@ -53,10 +62,11 @@ def test_gelu_bf16_against_the_oracle(cv):
     got = out.float().cpu().numpy().astype(np.float64)
     g = onum.gelu_tanh(x.astype(np.float64))
     want = onum.bf16_round(g)
-    # tanhf and the fp32 polynomial: relative error a few units of 2^-24
-    tie = tie_mask(g, 2.0 ** -19)
-    assert np.array_equal(got[~tie], want[~tie])
-    assert np.all(np.abs(got - g)[tie] <= 0.5 * spacing(got[tie]) + 2.0 ** -19 * np.abs(g[tie]) + 1e-30)
+    rel = gelu_rel_err(x.astype(np.float64))
+    tie = tie_mask(g, rel)
+    bad = np.nonzero((got != want) & ~tie)[0]
+    assert bad.size == 0, [(float(x[i]), got[i], want[i]) for i in bad[:8]]
+    assert np.all(np.abs(got - g)[tie] <= 0.5 * spacing(got[tie]) + rel[tie] * np.abs(g[tie]) + 1e-30)
     print(f"gelu: {int(tie.sum())} of {len(x)} values within the fp32 error of a bf16 midpoint")
 
 
@@ -84,7 +94,7 @@ def test_selfcond_mlp_stage(cv):
     # or gelu's own can reach the midpoint
     sp = spacing(onum.bf16_round(g))
     frac = np.abs((np.abs(g) / sp) % 1.0 - 0.5) * sp
-    tie = frac <= 1.13 * hb + 2.0 ** -19 * np.abs(g) + 1e-30
+    tie = frac <= 1.13 * hb + gelu_rel_err(h) * np.abs(g) + 1e-30
     gb = onum.bf16_round(g)
     bound = (H * U / (1 - H * U)) * ((np.abs(gb) + tie * sp) @ np.abs(W2).T) + (tie * sp) @ np.abs(W2).T
     err = np.abs(got - want)

@@ -802,3 +802,63 @@ def test_selfcond_mlp_maps_zero_to_zero_and_is_the_plain_composition():
                 acc += W2[j, k] * onum.bf16_round(onum.gelu_tanh(h))
             want[r, j] = acc
     np.testing.assert_allclose(oloop.selfcond_mlp(s, W1, W2), want, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- mixture of experts
+def _tiny_moe(seed=3, R=5, D=8, E=6, F=4, Fs=3):
+    rng = np.random.default_rng(seed)
+    q = lambda *s: onum.bf16_round(rng.standard_normal(s) / 2)  # noqa: E731
+    return dict(x=q(R, D), router=q(E, D), Wg=q(E * F, D), Wu=q(E * F, D), Wd=q(E * D, F),
+                shared=(q(Fs, D), q(Fs, D), q(D, Fs)), E=E, F=F, D=D)
+
+
+def test_moe_routing_by_hand():
+    from oracle import moe as omoe
+    x = np.array([[1.0, 0.0], [0.0, 1.0]])
+    router = np.array([[3.0, 0.0], [1.0, 1.0], [0.0, 2.0], [1.0, 0.0]])   # scores: row0 3,1,0,1 ; row1 0,1,2,0
+    chosen, w, margin = omoe.route(x, router, 2)
+    np.testing.assert_array_equal(chosen, [[0, 1], [2, 1]])   # row 0: 1 and 3 tie at 1 -> lower index 1
+    np.testing.assert_allclose(w[0], [np.e ** 3 / (np.e ** 3 + np.e), np.e / (np.e ** 3 + np.e)], rtol=1e-14)
+    assert margin[0] == 0.0 and margin[1] == 1.0
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-14)
+    _, ws, _ = omoe.route(x, router, 2, scale=np.array([2.0, 0.5, 1.0, 1.0]))
+    np.testing.assert_allclose(ws[0], w[0] * [2.0, 0.5], rtol=1e-14)
+
+
+def test_moe_brute_force_and_special_cases():
+    from oracle import moe as omoe
+    m = _tiny_moe()
+    x, D, F, E = m["x"], m["D"], m["F"], m["E"]
+    out, (chosen, w, _) = omoe.moe(x, m["router"], 3, m["Wg"], m["Wu"], m["Wd"], shared=m["shared"])
+    # element by element, straight from the definition
+    want = np.zeros_like(out)
+    for t in range(x.shape[0]):
+        s = [sum(x[t, i] * m["router"][e, i] for i in range(D)) for e in range(E)]
+        top = sorted(range(E), key=lambda e: (-s[e], e))[:3]
+        z = sum(math.exp(s[e] - s[top[0]]) for e in top)
+        for e in top:
+            we = math.exp(s[e] - s[top[0]]) / z
+            for o in range(D):
+                acc = 0.0
+                for f in range(F):
+                    hg = sum(m["Wg"][e * F + f, i] * x[t, i] for i in range(D))
+                    hu = sum(m["Wu"][e * F + f, i] * x[t, i] for i in range(D))
+                    acc += m["Wd"][e * D + o, f] * onum.bf16_round(onum.gelu_tanh(hg) * hu)
+                want[t, o] += we * acc
+        Wsg, Wsu, Wsd = m["shared"]
+        for o in range(D):
+            want[t, o] += sum(Wsd[o, f] * onum.bf16_round(onum.gelu_tanh(sum(Wsg[f, i] * x[t, i] for i in range(D)))
+                                                            * sum(Wsu[f, i] * x[t, i] for i in range(D)))
+                              for f in range(Wsg.shape[0]))
+    np.testing.assert_allclose(out, want, rtol=1e-10, atol=1e-12)
+    # zero input -> zero output (no biases anywhere)
+    z, _ = omoe.moe(np.zeros_like(x), m["router"], 3, m["Wg"], m["Wu"], m["Wd"], shared=m["shared"])
+    assert np.all(z == 0.0)
+    # k = E with one expert's weights doubled in W_down doubles only that expert's share
+    o1, (c1, w1, _) = omoe.moe(x, m["router"], E, m["Wg"], m["Wu"], m["Wd"])
+    Wd2 = m["Wd"].copy()
+    Wd2[2 * D:3 * D] *= 2
+    o2, _ = omoe.moe(x, m["router"], E, m["Wg"], m["Wu"], Wd2)
+    y2 = omoe.gated_mlp(x, m["Wg"][2 * F:3 * F], m["Wu"][2 * F:3 * F], m["Wd"][2 * D:3 * D])
+    share = np.array([w1[t, list(c1[t]).index(2)] for t in range(x.shape[0])])
+    np.testing.assert_allclose(o2 - o1, share[:, None] * y2, rtol=1e-10, atol=1e-12)
