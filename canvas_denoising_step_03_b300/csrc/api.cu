@@ -322,7 +322,8 @@ AttnPlan plan_attn(int dtype, int B, int C, int Hq, int Hkv, int d, int max_pref
     if (layer_type == CANVAS_LAYER_SLIDING && window > 0) keys = std::min(keys, window + kAttnBM + 64);
     keys += 64 + p.Tpad;
     const int nblk = (keys + kAttnBN - 1) / kAttnBN;
-    p.nsplit = std::max(1, std::min(kNumSms / std::max(1, units), nblk / 2));
+    // (at most 32 splits: the combine holds one split per lane)
+    p.nsplit = std::max(1, std::min(std::min(kNumSms / std::max(1, units), nblk / 2), 32));
   }
   return p;
 }

@@ -1049,8 +1049,11 @@ __global__ void __launch_bounds__(kThreads4, 1)
 }
 
 // One warp per output row (b, KV head, packed row g*C + i), eight rows per
-// block: merges the KV splits' partial rows by their running max and sum,
-// four consecutive columns per lane and step (16-byte loads).
+// block: merges the KV splits' partial rows by their running max and sum.
+// Lane s reads split s's (max, sum) and the warp shares them; each lane then
+// owns four consecutive columns per 128-column step and issues the loads of
+// every split before it adds them (in split order).
+constexpr int kMaxCombineSplits = 32;
 __global__ void __launch_bounds__(256) attention_combine_kernel(AttnTcArgs a) {
   const int GC = a.G * a.C;
   const int lane = threadIdx.x & 31;
@@ -1062,27 +1065,41 @@ __global__ void __launch_bounds__(256) attention_combine_kernel(AttnTcArgs a) {
   const int g = row / a.C, i = row % a.C;
   const size_t rows_per_split = (size_t)a.B * a.Hkv * a.q_tiles * kAttnBM;
   const size_t prow0 = (size_t)grp * a.q_tiles * kAttnBM + row;
-  float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.part_ml[(s * rows_per_split + prow0) * 2]);
-  float L = 0.f;
-  for (int s = 0; s < a.nsplit; ++s) {
-    const float ms = a.part_ml[(s * rows_per_split + prow0) * 2];
-    if (ms != -INFINITY) L += exp2f(ms - M) * a.part_ml[(s * rows_per_split + prow0) * 2 + 1];
+  const int ns = min(a.nsplit, kMaxCombineSplits);
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < ns) {
+    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (lane * rows_per_split + prow0) * 2);
+    ms = ml.x;
+    ls = ml.y;
   }
+  float M = ms;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // this lane's split weight 2^(m_s - M) (0 for an empty split), summed in split order
+  const float wl = ms == -INFINITY ? 0.f : exp2f(ms - M);
+  float L = 0.f;
+  for (int sp = 0; sp < ns; ++sp) L += __shfl_sync(0xffffffffu, wl * ls, sp);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int h = hk * a.G + g;
   __nv_bfloat16* dst = a.out + ((size_t)b * a.C + i) * a.Hq * a.d + (size_t)h * a.d;
   for (int c = lane * 4; c < a.d; c += 128) {
+    float4 v[kMaxCombineSplits < 8 ? kMaxCombineSplits : 8];
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float ms = a.part_ml[(s * rows_per_split + prow0) * 2];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      const float4 v = *reinterpret_cast<const float4*>(a.part_o + (s * rows_per_split + prow0) * a.d + c);
-      o[0] = fmaf(w, v.x, o[0]);
-      o[1] = fmaf(w, v.y, o[1]);
-      o[2] = fmaf(w, v.z, o[2]);
-      o[3] = fmaf(w, v.w, o[3]);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < ns)
+          v[j] = *reinterpret_cast<const float4*>(a.part_o + ((s0 + j) * rows_per_split + prow0) * a.d + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = __shfl_sync(0xffffffffu, wl, (s0 + j) & 31);
+        if (s0 + j < ns && w != 0.f) {
+          o[0] = fmaf(w, v[j].x, o[0]);
+          o[1] = fmaf(w, v[j].y, o[1]);
+          o[2] = fmaf(w, v[j].z, o[2]);
+          o[3] = fmaf(w, v[j].w, o[3]);
+        }
+      }
     }
     *reinterpret_cast<uint2*>(dst + c) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
   }

@@ -79,4 +79,9 @@ def gelu_tanh(x) -> np.ndarray:
     glossary, self-conditioning: "a small MLP" that maps zero to zero; the
     pages name no activation, and this is the Gemma family's)."""
     x = np.asarray(x, dtype=np.float64)
-    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+    u = np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)
+    # 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)): the same function, without the
+    # cancellation of 1 + tanh(u) for u << 0 (there tanh(u) rounds to -1 in
+    # fp64 once x < -6.5 or so)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-2.0 * u))

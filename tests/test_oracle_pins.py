@@ -782,6 +782,12 @@ def test_gelu_tanh_form_against_the_exact_gelu_and_its_symmetry():
     np.testing.assert_allclose(g - onum.gelu_tanh(-x), x, rtol=1e-13, atol=1e-14)
     assert onum.gelu_tanh(0.0) == 0.0
     assert abs(onum.gelu_tanh(20.0) - 20.0) < 1e-12 and abs(onum.gelu_tanh(-20.0)) < 1e-12
+    # far in the negative tail the value is x e^{2u} to leading order (not 0):
+    # relative accuracy is kept where 1 + tanh(u) would cancel
+    for xv in (-7.0, -9.0, -12.0):
+        u = math.sqrt(2 / math.pi) * (xv + 0.044715 * xv ** 3)
+        lead = xv * math.exp(2 * u)
+        assert abs(onum.gelu_tanh(xv) - lead) <= 1e-6 * abs(lead)
 
 
 def test_selfcond_mlp_maps_zero_to_zero_and_is_the_plain_composition():
