@@ -26,6 +26,36 @@ namespace {
 
 thread_local std::string t_last_error;
 
+// A side stream (non-blocking) and a fork / join event pair per host thread
+// and device, created on first use and kept for the life of the thread: work
+// that does not depend on the call's earlier kernels runs beside them, and
+// the call's stream waits for it before anything that needs it.  Recording
+// and waiting on events brings the side stream into a stream capture like
+// any fork / join.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+constexpr int kMaxSideDevices = 64;
+thread_local SideStream t_side[kMaxSideDevices];
+
+SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+  SideStream& x = t_side[dev];
+  if (!x.tried) {
+    x.tried = true;
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();  // not sticky: the calls then run everything in order on their stream
+      x.s = nullptr;
+    }
+  }
+  return x.s ? &x : nullptr;
+}
+
 // per-thread timing events (canvas_profile_events)
 struct EventPair {
   cudaEvent_t start = nullptr, stop = nullptr;
@@ -621,8 +651,43 @@ static canvas_status attention_impl(const void* x, int dtype, int B, int C, int 
   const int M = B * C;
   const int G = Hq / Hkv;
 
-  // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
   mark_start(CANVAS_KERNEL_PREP, stream);
+  // 3. prefix keys of global layers, the prefix rows of the tail, zero padding:
+  // independent of the projections and of the canvas rows (it writes other
+  // rows of the tail buffers), so it runs on a side stream beside steps 1-2
+  SideStream* side = side_stream();
+  cudaStream_t kstream = stream;
+  if (side) {
+    CANVAS_CUDA(cudaEventRecord(side->fork, stream));
+    CANVAS_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    kstream = side->s;
+  }
+  KeyPrepArgs k;
+  k.k_pool = kv->k_pool;
+  k.v_pool = kv->v_pool;
+  k.block_table = kv->block_table;
+  k.max_pages = kv->max_pages_per_seq;
+  k.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;
+  k.num_pages = kv->num_pages;
+  k.gamma_k = gamma_k;
+  k.freq = freq;
+  k.prefix_len = prefix_len;
+  k.B = B;
+  k.C = C;
+  k.Hkv = Hkv;
+  k.d = d;
+  k.max_prefix = max_prefix;
+  k.Tpad = pl.Tpad;
+  k.eps = eps;
+  k.global = global ? 1 : 0;
+  k.Kt = Kt;
+  k.vs_pre = vs_pre;
+  k.Kx = Kx;
+  k.Vx = Vx;
+  k.vs_tail = vs_tail;
+  CANVAS_CUDA(launch_key_prep(k, bf16, kstream));
+  if (side) CANVAS_CUDA(cudaEventRecord(side->join, kstream));
+  // 1. projections q = x W_q^T, k = x W_k^T, v = x W_v^T (fp32 accumulate)
   int proj_splits = 1;
   if (bf16) {
     // one launch for the two or three products (they share x)
@@ -665,31 +730,8 @@ static canvas_status attention_impl(const void* x, int dtype, int B, int C, int 
   p.Vx = Vx;
   p.vs_tail = vs_tail;
   CANVAS_CUDA(launch_prologue(p, bf16, stream));
-  // 3. prefix keys of global layers, the prefix rows of the tail, zero padding
-  KeyPrepArgs k;
-  k.k_pool = kv->k_pool;
-  k.v_pool = kv->v_pool;
-  k.block_table = kv->block_table;
-  k.max_pages = kv->max_pages_per_seq;
-  k.page_tokens = max_prefix > 0 ? kv->page_tokens : 64;
-  k.num_pages = kv->num_pages;
-  k.gamma_k = gamma_k;
-  k.freq = freq;
-  k.prefix_len = prefix_len;
-  k.B = B;
-  k.C = C;
-  k.Hkv = Hkv;
-  k.d = d;
-  k.max_prefix = max_prefix;
-  k.Tpad = pl.Tpad;
-  k.eps = eps;
-  k.global = global ? 1 : 0;
-  k.Kt = Kt;
-  k.vs_pre = vs_pre;
-  k.Kx = Kx;
-  k.Vx = Vx;
-  k.vs_tail = vs_tail;
-  CANVAS_CUDA(launch_key_prep(k, bf16, stream));
+  // 3. (launched first, beside steps 1-2) the prefix keys
+  if (side) CANVAS_CUDA(cudaStreamWaitEvent(stream, side->join, 0));
   mark_stop(CANVAS_KERNEL_PREP, stream);
 
   // 4. attention
