@@ -864,7 +864,9 @@ def run_reference(args, rank, world):
     return {"metric": METRIC, "value": v, "unit": "canvas steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded draws)", "impl": "reference",
-            "config": {"workload": WORKLOAD}, "cpu_baseline": {"value": v, "unit": "canvas steps/s", "cores": cores,
+            "config": {"workload": WORKLOAD, "l2": "flushed between timed steps (252 MB write, outside the step events)",
+                       "parallelism": f"replicas x{world} (independent canvases per GPU)"},
+            "cpu_baseline": {"value": v, "unit": "canvas steps/s", "cores": cores,
                                                               "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "canvas steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -157,7 +157,8 @@ def test_full_vocab_workload(cv):
     runb = SampleRun(cv, s)  # repeat: bit-identical
     assert torch.equal(run.soft, runb.soft) and torch.equal(run.tokens, runb.tokens)
     logits = wl.as_f64(s.logits, "bf16")
-    soft_rows = [0, 1, 2, 100, 128, 200, 254, 255]
+    soft_rows = sorted(set([0, 1, 2, 100, 128, 200, 254, 255] +
+                           list(np.random.default_rng(31).choice(256, 24, replace=False))))
     ref = osamp.canvas_sample(logits, None, c.bound, c.seed, c.step, canvas_len=c.C, probs_storage="bf16")
     # soft embedding of sampled rows, streaming E in fp64 chunks
     want = np.zeros((len(soft_rows), c.D))
@@ -169,6 +170,13 @@ def test_full_vocab_workload(cv):
     ref["soft_emb"] = soft_full
     assert 0.3 < ref["commit_mask"].mean() < 0.7
     compare(cv, s, run, ref, soft_rows=soft_rows)
+    # the bf16 probabilities of those rows element by element: each a correct
+    # rounding of a value within the path's fp32 error of the exact one
+    runp = SampleRun(cv, s, probs_dtype="bf16")
+    got = runp.probs.float().cpu().numpy()[soft_rows].astype(np.float64)
+    exact = osamp.canvas_sample(logits[soft_rows], None, c.bound, c.seed, c.step, canvas_len=c.C)["probs"]
+    bar = 0.5 * onum_spacing(exact) + 2.0 ** -17 * exact
+    assert np.all(np.abs(got - exact) <= bar), float(np.max(np.abs(got - exact) - bar))
 
 
 @pytest.mark.parametrize("V", [262144, 262136])   # every slice full / a shorter last slice
