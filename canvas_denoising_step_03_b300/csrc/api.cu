@@ -146,6 +146,29 @@ canvas_status make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, ui
   return CANVAS_OK;
 }
 
+// The same bf16 [rows][cols] tensor seen as [cols / 64][rows][64] (dimension
+// strides: row = the row pitch, chunk = 128 bytes), box {64, box_rows,
+// box_chunks}: one copy lands box_chunks 64-column tiles of box_rows rows,
+// tile after tile, each laid out (and 128-byte swizzled) exactly as a 2D box
+// of {64, box_rows} would be.
+canvas_status make_map_bf16_chunked(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                                    uint32_t box_rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0)
+    return fail(CANVAS_ERR_ARG, "tensor base address must be 16-byte aligned");
+  if (cols % 64 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "chunked view needs a multiple of 64 columns");
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CANVAS_ERR_CUDA, "cuTensorMapEncodeTiled (chunked view) failed (%d)", int(r));
+  return CANVAS_OK;
+}
+
 // fp32 [z][rows][cols] (row pitch ld elements, slab pitch rows * ld) for TMA
 // stores of 32 x 32 boxes with the 128-byte swizzle; stores clip at every
 // edge, so no box spills into the next row block or slab.
@@ -755,22 +778,30 @@ static canvas_status attention_impl(const void* x, int dtype, int B, int C, int 
       maps.kpre = maps.kx;  // never read: no prefix sub-blocks
       maps.vpre = maps.vx;
     }
-    // the 4-SM kernel (head_dim 512) reads keys in 32-row boxes
+    // the 4-SM kernel (head_dim 512) reads keys in boxes of 32 rows x all of
+    // d and values in boxes of 64 rows x 128 columns, one copy each
     const bool quad = d == 512;
     if (quad) {
-      st = make_map_bf16(&maps.kx32, Kx, BH * pl.Tpad, d, 32, 64);
+      st = make_map_bf16_chunked(&maps.kx_c, Kx, BH * pl.Tpad, d, 32, 8);
+      if (st != CANVAS_OK) return st;
+      st = make_map_bf16_chunked(&maps.vx_c, Vx, BH * pl.Tpad, d, 64, 2);
       if (st != CANVAS_OK) return st;
       if (max_prefix > 0) {
         const uint64_t pool_rows = uint64_t(kv->num_pages) * Hkv * kv->page_tokens;
-        st = global ? make_map_bf16(&maps.kpre32, Kt, BH * max_prefix, d, 32, 64)
-                    : make_map_bf16(&maps.kpre32, kv->k_pool, pool_rows, d, 32, 64);
+        st = global ? make_map_bf16_chunked(&maps.kpre_c, Kt, BH * max_prefix, d, 32, 8)
+                    : make_map_bf16_chunked(&maps.kpre_c, kv->k_pool, pool_rows, d, 32, 8);
+        if (st != CANVAS_OK) return st;
+        st = make_map_bf16_chunked(&maps.vpre_c, global ? kv->k_pool : kv->v_pool, pool_rows, d, 64, 2);
         if (st != CANVAS_OK) return st;
       } else {
-        maps.kpre32 = maps.kx32;
+        maps.kpre_c = maps.kx_c;  // never read: no prefix sub-blocks
+        maps.vpre_c = maps.vx_c;
       }
     } else {
-      maps.kx32 = maps.kx;  // not read by the other kernels
-      maps.kpre32 = maps.kpre;
+      maps.kx_c = maps.kx;  // not read by the other kernels
+      maps.vx_c = maps.vx;
+      maps.kpre_c = maps.kpre;
+      maps.vpre_c = maps.vpre;
     }
     AttnTcArgs t;
     t.B = B;

@@ -575,13 +575,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (d 0..127) sits in TMEM and the ring has three stages; with two, half of Q
 // sits in TMEM and the ring has four stages (two blocks of K and V in flight).
 // TMEM columns: O [0, 256), S / P NS x 64 from 256, Q at 256 + 64 NS.
-// The ring is split in two: NST - 1 stages of K, loaded by warp 0 in block
-// order, and one stage of V, loaded by warp 6 -- so the keys of the next
+// The ring is split in two: NST - VS stages of K, loaded by warp 0 in block
+// order, and VS stages of V, loaded by warp 6 -- so the keys of the next
 // blocks' S are fetched as soon as an S has consumed its stage, without
-// queueing behind the values of the current block.
-template <int NS>
+// queueing behind the values of the current block.  With two V stages the
+// values of block n + 1 load while block n's P.V waits for its P (with one,
+// every block waited for its values to arrive after the previous P.V).
+template <int NS, int VS>
 struct Cfg4 {
   static constexpr int NST = NS == 2 ? 4 : 3;
+  static constexpr int KR = NST - VS;  // K stages [0, KR), V stages [KR, NST)
+  static_assert(VS >= 1 && KR >= 2, "ring split");
   static constexpr int QT = NS == 2 ? 4 : 2;        // 64-wide chunks of Q held in TMEM
   static constexpr int QSBytes = (8 - QT) * 16384;  // the other chunks in shared memory (128 rows each)
   static constexpr int POBytes = 16384;      // the partner's P: 128 rows x 64 keys bf16
@@ -589,10 +593,10 @@ struct Cfg4 {
 };
 constexpr int kThreads4 = 224;  // K TMA warp, MMA warp, 4 softmax / epilogue warps, V TMA warp
 
-template <int NS>
+template <int NS, int VS>
 __global__ void __launch_bounds__(kThreads4, 1)
     attention_tc4_kernel(const __grid_constant__ AttnTcMaps maps, AttnTcArgs a) {
-  using K = Cfg4<NS>;
+  using K = Cfg4<NS, VS>;
   constexpr int D = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -659,10 +663,10 @@ __global__ void __launch_bounds__(kThreads4, 1)
     flags[0] = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&maps.q);
-    tma_prefetch_desc(&maps.kpre32);
-    tma_prefetch_desc(&maps.vpre);
-    tma_prefetch_desc(&maps.kx32);
-    tma_prefetch_desc(&maps.vx);
+    tma_prefetch_desc(&maps.kpre_c);
+    tma_prefetch_desc(&maps.vpre_c);
+    tma_prefetch_desc(&maps.kx_c);
+    tma_prefetch_desc(&maps.vx_c);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -674,21 +678,21 @@ __global__ void __launch_bounds__(kThreads4, 1)
   const uint32_t tmem = *tmem_slot;
   constexpr uint32_t kColS = 256, kColQ = 256 + 64 * NS;
 
-  constexpr int KR = K::NST - 1;  // K stages [0, KR), the V stage KR
+  constexpr int KR = K::KR;
   auto row_of = [&](int sb, bool key, const CUtensorMap*& map) -> int {
     if (sb < sq.n_pre) {
       const int pos = sq.s0 + 64 * sb;
-      map = key ? &maps.kpre32 : &maps.vpre;
+      map = key ? &maps.kpre_c : &maps.vpre_c;
       return (key && !a.kpre_paged) ? grp * a.max_prefix + pos : paged_row(a, b, hk, pos);
     }
-    map = key ? &maps.kx32 : &maps.vx;
+    map = key ? &maps.kx_c : &maps.vx_c;
     return grp * a.Tpad + 64 * (sb - sq.n_pre);
   };
   if (warp == 0 || warp == 6) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producers (every CTA): K (warp 0), V (warp 6)
       const bool kp = warp == 0;
-      const int nst = kp ? KR : 1, s0 = kp ? 0 : KR;
+      const int nst = kp ? KR : VS, s0 = kp ? 0 : KR;
       if (kp) {
         const uint32_t lead_q = mapa_shared(smem_u32(q_full), lead_rank);
         if (leader) mbar_arrive_expect_tx(q_full, uint32_t(2 * K::QSBytes));
@@ -703,17 +707,19 @@ __global__ void __launch_bounds__(kThreads4, 1)
         uint8_t* dst = ring + s * kStageBytes;
         const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead_rank);
         if (kp) {
-          // this CTA's 32 keys of the pair's key half, all of d: 8 chunks of 4 KB
+          // this CTA's 32 keys of the pair's key half, all of d: 8 chunks of
+          // 4 KB in one copy
           const CUtensorMap* map;
           const int row = row_of(2 * (sq.kb0 + n) + pp, true, map) + 32 * h;
-          for (int c = 0; c < 8; ++c) tma_load_2d_pair(dst + c * 4096, map, bar, c * 64, row);
+          tma_load_3d_pair(dst, map, bar, 0, row, 0);
         } else {
-          // all 128 keys of block n, this CTA's 128 columns of value half pp
+          // all 128 keys of block n, this CTA's 128 columns of value half pp:
+          // per 64-key sub-block u one copy of two 64-column chunks (16 KB at
+          // u * 16 KB, chunk after chunk)
           for (int u = 0; u < 2; ++u) {
             const CUtensorMap* map;
             const int row = row_of(2 * (sq.kb0 + n) + u, false, map);
-            for (int c = 0; c < 2; ++c)
-              tma_load_2d_pair(dst + c * 16384 + u * 8192, map, bar, pp * 256 + h * 128 + c * 64, row);
+            tma_load_3d_pair(dst + u * 16384, map, bar, 0, row, pp * 4 + h * 2);
           }
         }
       }
@@ -732,10 +738,10 @@ __global__ void __launch_bounds__(kThreads4, 1)
       const uint32_t q_base = smem_u32(sQ);
       bool alive = mbar_wait(q_full, 0, flags) && mbar_wait(qt_ready, 0, flags);
       tc_fence_after();
-      // K of block n: stage n % KR; V of block n: stage KR
+      // K of block n: stage n % KR; V of block n: stage KR + n % VS
       auto consume = [&](int n, bool key) -> uint32_t {
-        const int s = key ? n % KR : KR;
-        const uint32_t par = key ? (n / KR) & 1 : n & 1;
+        const int s = key ? n % KR : KR + n % VS;
+        const uint32_t par = key ? (n / KR) & 1 : (n / VS) & 1;
         if (!mbar_wait(&full[s], par, flags)) {
           alive = false;
           return 0;
@@ -771,11 +777,11 @@ __global__ void __launch_bounds__(kThreads4, 1)
         const uint32_t tS = tmem + kColS + (n % NS) * 64;
         const uint32_t st = consume(n, false);
         if (!alive) return;
-        const uint64_t v_desc0 = smem_desc_sw128(st, 16384, 1024);
+        const uint64_t v_desc0 = smem_desc_sw128(st, 8192, 1024);
         const uint64_t a_desc0 = po_desc0 + uint64_t(((n & 1) * K::POBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma2_bf16_ts(tmem, tS + kk * 8, v_desc0 + uint64_t((pp * 8192 + kk * 2048) >> 4), idesc_pv,
+          mma2_bf16_ts(tmem, tS + kk * 8, v_desc0 + uint64_t((pp * 16384 + kk * 2048) >> 4), idesc_pv,
                        (n | kk) != 0 ? 1u : 0u);
         // the other pair's keys once its P has landed in both CTAs
         if (!mbar_wait(&px_full[n % NS], (n / NS) & 1, flags)) {
@@ -786,8 +792,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma2_bf16_ss(tmem, a_desc0 + uint64_t((kk * 32) >> 4),
-                       v_desc0 + uint64_t(((1 - pp) * 8192 + kk * 2048) >> 4), idesc_pv, 1u);
-        mma2_commit_mc(&empty[KR], pair_mask);
+                       v_desc0 + uint64_t(((1 - pp) * 16384 + kk * 2048) >> 4), idesc_pv, 1u);
+        mma2_commit_mc(&empty[KR + n % VS], pair_mask);
         mma2_commit_mc(&pv_done[n & 1], 0xF);
       };
       for (int n = 0; n < NS && n < nb && alive; ++n) qk(n);
@@ -1125,12 +1131,16 @@ cudaError_t launch_d(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t s
 #ifndef CANVAS_QUAD_S_BUFFERS
 #define CANVAS_QUAD_S_BUFFERS 2
 #endif
+#ifndef CANVAS_QUAD_V_STAGES
+#define CANVAS_QUAD_V_STAGES 2
+#endif
 cudaError_t launch_quad(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream) {
-  constexpr int NS = CANVAS_QUAD_S_BUFFERS;
+  constexpr int NS = CANVAS_QUAD_S_BUFFERS, VS = CANVAS_QUAD_V_STAGES;
   static bool attr_set = false;
-  const int smem = Cfg4<NS>::Smem;
+  const int smem = Cfg4<NS, VS>::Smem;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_tc4_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(attention_tc4_kernel<NS, VS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1147,7 +1157,7 @@ cudaError_t launch_quad(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc4_kernel<NS>, maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_tc4_kernel<NS, VS>, maps, a);
   count_launches(1);
   return e;
 }

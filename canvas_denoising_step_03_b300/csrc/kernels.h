@@ -199,7 +199,10 @@ struct AttnTcArgs {
 };
 struct AttnTcMaps {
   CUtensorMap q, kpre, vpre, kx, vx;
-  CUtensorMap kpre32, kx32;  // keys in 32-row boxes (the 4-SM kernel)
+  // the 4-SM kernel: 3D views [64-column chunk][row][64] of the same tensors,
+  // so one copy brings a key box of 32 rows x all eight chunks, or a value
+  // box of 64 rows x two chunks
+  CUtensorMap kpre_c, kx_c, vpre_c, vx_c;
 };
 size_t attention_tc_smem_bytes(int d);
 cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cudaStream_t stream);
