@@ -425,16 +425,28 @@ bool attn_shape_ok(int dtype, int B, int C, int D, int Hq, int Hkv, int d, int m
 
 // ------------------------------------------------------------------ sampler layout
 struct SampleLayout {
-  size_t probs, argmax, gemm, total;
+  size_t probs, argmax, gemm, states, total;
 };
 
 SampleLayout sample_layout(int dtype, int rows, int V, int D) {
   SampleLayout L;
   L.probs = size_t(rows) * V * (dtype == CANVAS_BF16 ? 2 : 4);
   L.argmax = size_t(rows) * 4;
-  L.gemm = dtype == CANVAS_BF16 ? gemm_ws_bytes(plan_gemm(rows, D, V)) : 0;
-  L.total = align_up(L.probs) + align_up(L.argmax) + align_up(L.gemm) + kAlign;
+  const GemmPlan gp = plan_gemm(rows, D, V);
+  L.gemm = dtype == CANVAS_BF16 ? gemm_ws_bytes(gp) : 0;
+  L.states = dtype == CANVAS_BF16 ? size_t(rows) * gp.splits * 8 * sizeof(float) : 0;
+  L.total = align_up(L.probs) + align_up(L.argmax) + align_up(L.gemm) + align_up(L.states) + kAlign;
   return L;
+}
+
+// The deferred-normalisation sampler applies when nobody reads the stored
+// probabilities themselves: bf16 logits, no probs_out, argmax commits, and a
+// soft-embedding GEMM split along the vocabulary into ranges one CTA stages.
+bool sample_deferred(int dtype, const void* probs_out, int commit_mode, const GemmPlan& gp) {
+  if (dtype != CANVAS_BF16 || probs_out != nullptr || (commit_mode & 2) != 0) return false;
+  if (gp.splits < 2 || gp.splits > kMaxSampleSlices) return false;
+  const long long longest = (long long)(gp.kblocks / gp.splits + (gp.kblocks % gp.splits ? 1 : 0)) * 64;
+  return longest <= kSampleSliceMaxElems;
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -1149,7 +1161,9 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
   char* probs_ws = cv.take<char>(L.probs);
   int32_t* argmax_ws = cv.take<int32_t>(L.argmax);
   void* gws = cv.take<char>(L.gemm);
+  float* states_ws = cv.take<float>(L.states);
   const bool bf16 = dtype == CANVAS_BF16;
+  const GemmPlan gp = plan_gemm(rows, D, V);
 
   SampleArgs a;
   a.rows = rows;
@@ -1184,6 +1198,34 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
     a.probs_f32 = (probs_out && probs_dtype == CANVAS_FP32) ? static_cast<float*>(probs_out)
                                                              : reinterpret_cast<float*>(probs_ws);
     if (probs_out && probs_dtype == CANVAS_BF16) a.probs_bf16 = static_cast<__nv_bfloat16*>(probs_out);
+  }
+  a.slices = 0;
+  a.kb_per = a.kb_rem = 0;
+  a.slice_state = nullptr;
+  if (sample_deferred(dtype, probs_out, commit_mode, gp)) {
+    // per-range p~ and states; the GEMM of p~ and E leaves its split
+    // partials; one pass merges the states, decides, and sums the partials
+    // scaled to probabilities
+    a.slices = gp.splits;
+    a.kb_per = gp.kblocks / gp.splits;
+    a.kb_rem = gp.kblocks % gp.splits;
+    a.slice_state = states_ws;
+    mark_start(CANVAS_KERNEL_SAMPLER, stream);
+    CANVAS_CUDA(launch_sampler_slices(a, logits, stream));
+    mark_stop(CANVAS_KERNEL_SAMPLER, stream);
+    mark_start(CANVAS_KERNEL_SOFT_EMB, stream);
+    float* partials = nullptr;
+    int splits = 0;
+    const void* Bs[1] = {E};
+    void* Cs[1] = {soft_emb};
+    const int Ns[1] = {D};
+    const canvas_status st =
+        run_gemm_group(a.probs_bf16, Bs, Cs, Ns, 1, 1, rows, V, 0, 0, gws, stream, &partials, &splits);
+    if (st != CANVAS_OK) return st;
+    if (splits != a.slices) return fail(CANVAS_ERR_CUDA, "canvas_sample: GEMM split plan changed");
+    CANVAS_CUDA(launch_soft_reduce(a, partials, soft_emb, D, stream));
+    mark_stop(CANVAS_KERNEL_SOFT_EMB, stream);
+    return CANVAS_OK;
   }
   mark_start(CANVAS_KERNEL_SAMPLER, stream);
   CANVAS_CUDA(launch_sampler(a, logits, bf16, stream));

@@ -32,9 +32,22 @@ struct SampleArgs {
   int32_t* argmax;
   __nv_bfloat16* probs_bf16;
   float* probs_f32;
+  // deferred normalisation (launch_sampler_slices): the vocabulary ranges
+  // are the soft-embedding GEMM's K splits (kb_per or kb_per + 1 blocks of 64)
+  int slices, kb_per, kb_rem;
+  float* slice_state;  // [rows][slices][8]: m, Z, T, best logit, argmax (int bits)
 };
 
+// Largest vocabulary range one sampler CTA stages in shared memory (entries),
+// and the most ranges per row of the deferred path.
+constexpr int kSampleSliceMaxElems = 32768;
+constexpr int kMaxSampleSlices = 148;
+
 cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, cudaStream_t stream);
+// deferred path: per-range states and p~ (bf16 logits), then, after the
+// GEMM of p~ and E, the row outputs / decisions and the scaled split sum
+cudaError_t launch_sampler_slices(const SampleArgs& a, const void* logits, cudaStream_t stream);
+cudaError_t launch_soft_reduce(const SampleArgs& a, const float* partials, float* soft, int D, cudaStream_t stream);
 
 // ----------------------------------------------------------------- GEMMs
 // tcgen05 bf16 GEMM, up to three problems sharing A and K (the q / k / v

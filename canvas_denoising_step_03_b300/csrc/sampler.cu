@@ -218,7 +218,7 @@ __device__ __forceinline__ RowState reduce_row(RowState s, RowState* warp_part, 
 // needs no cluster-wide barrier; one cluster barrier, split into an arrive
 // after the exchange and a wait before exit, keeps every CTA alive until all
 // stores into it have landed.
-constexpr int kSmemSliceBytes = 65536;   // largest staged slice
+constexpr int kSmemSliceBytes = kSampleSliceMaxElems * 2;  // largest staged slice
 constexpr int kPieceElems = 8192;
 constexpr int kMaxPieces = kSmemSliceBytes / (2 * kPieceElems);
 
@@ -420,6 +420,197 @@ __global__ void __launch_bounds__(kThreads) sample_rows_smem_kernel(SampleArgs a
     }
   }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Deferred normalisation (bf16 logits, no probabilities requested, argmax
+// commits): the vocabulary of a row is cut into the K ranges of the
+// soft-embedding GEMM's splits, one CTA per (range, row) and no cluster.  A
+// CTA stages its range in shared memory as above, reduces it to its own
+// (m_s, Z_s, T_s, argmax) state, writes p~ = 2^(y - m_s) (<= 1) for its
+// range and stores the state; nothing waits for another CTA.  The row's
+// statistics and decision, and the factor 2^(m_s - m) / Z that turns each
+// range's p~ into probabilities, are applied after the GEMM, where its split
+// partials are summed (soft_reduce_kernel): P.E = sum_s 2^(m_s - m) / Z *
+// (p~_s . E_s).
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) sample_slices_kernel(SampleArgs a,
+                                                                  const __nv_bfloat16* __restrict__ logits) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kMaxK = kSmemSliceBytes / 16 / kThreads;  // 16-byte chunks per thread
+  constexpr int kKPerPiece = kPieceElems / 8 / kThreads;
+  static_assert(kKPerPiece >= 1 && kMaxK % kKPerPiece == 0, "piece layout");
+  extern __shared__ __align__(128) uint8_t slice_raw[];
+  __shared__ RowState warp_part[kWarps];
+  __shared__ uint64_t full[kMaxPieces];
+  __shared__ int abort_flag;
+  const int row = blockIdx.y, sl = blockIdx.x;
+  const long long kb0 = (long long)sl * a.kb_per + min(sl, a.kb_rem);
+  const long long c0 = kb0 * 64;
+  const long long c1 = min((long long)a.V, (kb0 + a.kb_per + (sl < a.kb_rem ? 1 : 0)) * 64);
+  const int n = c1 > c0 ? int(c1 - c0) : 0;  // a multiple of 8, at most kSmemSliceBytes / 2
+  const int nch = n / 8;
+  const __nv_bfloat16* src = logits + (long long)row * a.V + c0;
+  const uint4* slice4 = reinterpret_cast<const uint4*>(slice_raw);
+  if (threadIdx.x == 0) {
+    for (int p = 0; p < kMaxPieces; ++p) mbar_init(&full[p], 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+    for (int p = 0; p * kPieceElems < n; ++p) {
+      const uint32_t cnt = uint32_t(min(kPieceElems, n - p * kPieceElems));
+      mbar_arrive_expect_tx(&full[p], cnt * 2u);
+      bulk_load(slice_raw + p * kPieceElems * 2, src + p * kPieceElems, cnt * 2u, &full[p]);
+    }
+  }
+  __syncthreads();
+  const float ysc = a.inv_temp * kLog2e;
+  // (1) the thread's maximum and the first chunk that holds it
+  float bv = -INFINITY;
+  int bk = -1;
+#pragma unroll
+  for (int k = 0; k < kMaxK; ++k) {
+    if (k % kKPerPiece == 0 && (k / kKPerPiece) * kPieceElems < n) mbar_wait(&full[k / kKPerPiece], 0, &abort_flag);
+    const int j = int(threadIdx.x) + k * kThreads;
+    if (j < nch) {
+      const uint4 u = slice4[j];
+      const float gm = bf16x2_max(u.x, u.y, u.z, u.w);
+      if (gm > bv) {
+        bv = gm;
+        bk = k;
+      }
+    }
+  }
+  RowState s;
+  state_init(s);
+  if (bk >= 0) {
+    const int jb = int(threadIdx.x) + bk * kThreads;
+    const uint4 u = slice4[jb];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    int e = 7;
+#pragma unroll
+    for (int q = 3; q >= 0; --q) {
+      if (__uint_as_float(w[q] & 0xffff0000u) == bv) e = 2 * q + 1;
+      if (__uint_as_float(w[q] << 16) == bv) e = 2 * q;
+    }
+    s.bx = bv;
+    s.bi = int(c0) + 8 * jb + e;
+    // (2) Z and T about the thread's maximum, two logits per instruction
+    const float mt = bv * ysc;
+    const uint64_t ysc2 = f2_pack(ysc, ysc), nmt2 = f2_pack(-mt, -mt);
+    uint64_t Z2 = 0, T2 = 0;
+#pragma unroll 4
+    for (int k = 0; k < kMaxK; ++k) {
+      const int j = int(threadIdx.x) + k * kThreads;
+      if (j < nch) {
+        const uint4 v = slice4[j];
+        const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t t2 = f2_fma(f2_from_bf16x2(x4[q]), ysc2, nmt2);
+          const uint64_t e2 = f2_pack(ex2_approx(f2_lo(t2)), ex2_approx(f2_hi(t2)));
+          Z2 = f2_add(Z2, e2);
+          T2 = f2_fma(t2, e2, T2);
+        }
+      }
+    }
+    s.m = mt;
+    s.Z = f2_lo(Z2) + f2_hi(Z2);
+    s.T = f2_lo(T2) + f2_hi(T2);
+  }
+  // warp, then CTA (fixed order)
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    RowState o;
+    o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
+    o.Z = __shfl_xor_sync(0xffffffffu, s.Z, off);
+    o.T = __shfl_xor_sync(0xffffffffu, s.T, off);
+    o.bx = __shfl_xor_sync(0xffffffffu, s.bx, off);
+    o.bi = __shfl_xor_sync(0xffffffffu, s.bi, off);
+    RowState lo = (threadIdx.x & off) ? o : s;
+    const RowState hi = (threadIdx.x & off) ? s : o;
+    state_merge(lo, hi);
+    s = lo;
+  }
+  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RowState t = warp_part[0];
+    for (int w = 1; w < kWarps; ++w) state_merge(t, warp_part[w]);
+    float* st = a.slice_state + ((long long)row * a.slices + sl) * 8;
+    reinterpret_cast<float4*>(st)[0] = make_float4(t.m, t.Z, t.T, t.bx);
+    reinterpret_cast<int4*>(st)[1] = make_int4(t.bi, 0, 0, 0);
+    warp_part[0].m = t.m;
+  }
+  __syncthreads();
+  // p~ = 2^(y - m_s) (a range with no finite logit writes zeros)
+  const float ms = warp_part[0].m;
+  const bool live = ms != -INFINITY;
+  const uint64_t ysc2 = f2_pack(ysc, ysc), nms2 = f2_pack(-ms, -ms);
+  __nv_bfloat16* dst = a.probs_bf16 + (long long)row * a.V + c0;
+#pragma unroll 4
+  for (int k = 0; k < kMaxK; ++k) {
+    const int j = int(threadIdx.x) + k * kThreads;
+    if (j >= nch) break;
+    const uint4 u = slice4[j];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t t2 = f2_fma(f2_from_bf16x2(w[i]), ysc2, nms2);
+      q[i] = live ? pack_bf16x2(ex2_approx(f2_lo(t2)), ex2_approx(f2_hi(t2))) : 0u;
+    }
+    *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+// After the soft-embedding GEMM of the deferred path: one block per row
+// merges the row's range states in range order (the row's m, Z, T and
+// argmax, bit-identical whichever order the ranges ran in), writes the row
+// outputs and decision, and sums the GEMM's split partials in split order,
+// each scaled by 2^(m_s - m) / Z.
+__global__ void __launch_bounds__(256) soft_reduce_kernel(SampleArgs a, const float* __restrict__ partials,
+                                                          float* __restrict__ soft, int D) {
+  __shared__ float wgt[kMaxSampleSlices];
+  __shared__ RowState row_t;
+  const int row = blockIdx.x;
+  const float* st0 = a.slice_state + (long long)row * a.slices * 8;
+  if (threadIdx.x == 0) {
+    RowState t;
+    state_init(t);
+    for (int sl = 0; sl < a.slices; ++sl) {
+      const float4 v = reinterpret_cast<const float4*>(st0 + sl * 8)[0];
+      RowState o;
+      o.m = v.x;
+      o.Z = v.y;
+      o.T = v.z;
+      o.bx = v.w;
+      o.bi = reinterpret_cast<const int4*>(st0 + sl * 8)[1].x;
+      state_merge(t, o);
+    }
+    row_decision(a, row, t);
+    row_t = t;
+  }
+  __syncthreads();
+  const RowState t = row_t;
+  for (int sl = threadIdx.x; sl < a.slices; sl += blockDim.x) {
+    const float ms = st0[sl * 8], zs = st0[sl * 8 + 1];
+    wgt[sl] = (zs > 0.f && t.Z > 0.f) ? ex2_approx(ms - t.m) / t.Z : 0.f;
+  }
+  __syncthreads();
+  const long long plane = (long long)a.rows * D / 4;  // float4s per split slab
+  const float4* p4 = reinterpret_cast<const float4*>(partials) + (long long)row * D / 4;
+  float4* o4 = reinterpret_cast<float4*>(soft) + (long long)row * D / 4;
+  for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < a.slices; ++sl) {
+      const float4 v = __ldcs(p4 + sl * plane + c);
+      const float w = wgt[sl];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    o4[c] = acc;
+  }
 }
 
 template <typename T, int kThreads>
@@ -624,6 +815,34 @@ cudaError_t launch_sampler(const SampleArgs& a, const void* logits, bool bf16, c
     count_launches(1);
   }
   return e;
+}
+
+cudaError_t launch_sampler_slices(const SampleArgs& a, const void* logits, cudaStream_t stream) {
+  constexpr int kThreads = 256;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(sample_slices_kernel<kThreads>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemSliceBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long elems = ((long long)a.kb_per + (a.kb_rem > 0 ? 1 : 0)) * 64;
+  const size_t smem = size_t(min((long long)a.V, elems)) * 2;
+  sample_slices_kernel<kThreads><<<dim3(a.slices, a.rows, 1), kThreads, smem, stream>>>(
+      a, static_cast<const __nv_bfloat16*>(logits));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_soft_reduce(const SampleArgs& a, const float* partials, float* soft, int D, cudaStream_t stream) {
+  soft_reduce_kernel<<<a.rows, 256, 0, stream>>>(a, partials, soft, D);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !(a.commit_mode & 1)) return e;
+  const int n_canvas = a.rows / a.canvas_len;
+  commit_prefix_kernel<<<(n_canvas + 127) / 128, 128, 0, stream>>>(a, n_canvas);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace canvas

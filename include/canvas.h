@@ -252,8 +252,15 @@ size_t canvas_sample_workspace_size(int dtype, int rows, int V, int D);
  *   probs_out [rows, V] or NULL   out: softmax, in probs_dtype; 16-byte aligned
  *   probs_dtype                   CANVAS_BF16 or CANVAS_FP32
  *   soft_emb [rows, D] fp32       out: P.E, 16-byte aligned.  bf16 calls
- *                                 multiply the bf16 probabilities; fp32 calls
- *                                 the fp32 ones.
+ *                                 multiply bf16 probabilities; fp32 calls the
+ *                                 fp32 ones.  A bf16 call with probs_out NULL
+ *                                 and commit_mode bit 1 clear defers the
+ *                                 normalisation: each vocabulary range of the
+ *                                 product's K split stores bf16 2^(y - m_s)
+ *                                 against its own maximum m_s, and the split
+ *                                 sums are scaled by 2^(m_s - m) / Z (the same
+ *                                 product; the bf16 roundings fall on the
+ *                                 unnormalised values).
  *   workspace, ws_bytes           >= canvas_sample_workspace_size(...)
  *
  * Supported: V % 8 == 0, D % 8 == 0, rows >= 1.
