@@ -562,55 +562,94 @@ __global__ void __launch_bounds__(kThreads) sample_slices_kernel(SampleArgs a,
   }
 }
 
-// After the soft-embedding GEMM of the deferred path: one block per row
-// merges the row's range states in range order (the row's m, Z, T and
-// argmax, bit-identical whichever order the ranges ran in), writes the row
-// outputs and decision, and sums the GEMM's split partials in split order,
-// each scaled by 2^(m_s - m) / Z.
-__global__ void __launch_bounds__(256) soft_reduce_kernel(SampleArgs a, const float* __restrict__ partials,
-                                                          float* __restrict__ soft, int D) {
+// After the soft-embedding GEMM of the deferred path: a row's blocks (its D
+// columns cut into blockDim-wide float4 groups) each merge the row's range
+// states (warp 0: lane s holds range s, a fixed butterfly merges them, so the
+// row's m, Z, T and argmax are bit-identical in every block and whichever
+// order the ranges ran in); the first block writes the row outputs and
+// decision.  Every thread loads its four columns' split partials before the
+// merge (up to kSoftRegSplits of them held in registers) and then sums them
+// in split order, each scaled by 2^(m_s - m) / Z.
+constexpr int kSoftReduceThreads = 128;
+constexpr int kSoftRegSplits = 16;
+__global__ void __launch_bounds__(kSoftReduceThreads) soft_reduce_kernel(SampleArgs a,
+                                                                         const float* __restrict__ partials,
+                                                                         float* __restrict__ soft, int D) {
   __shared__ float wgt[kMaxSampleSlices];
-  __shared__ RowState row_t;
   const int row = blockIdx.x;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column
+  const bool col = c < D / 4;
+  const long long plane = (long long)a.rows * D / 4;  // float4s per split slab
+  const float4* p4 = reinterpret_cast<const float4*>(partials) + (long long)row * D / 4 + c;
+  float4 v[kSoftRegSplits];
+#pragma unroll
+  for (int j = 0; j < kSoftRegSplits; ++j)
+    if (col && j < a.slices) v[j] = __ldcs(p4 + j * plane);
   const float* st0 = a.slice_state + (long long)row * a.slices * 8;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    auto load_state = [&](int sl) {
+      RowState o;
+      const float4 f = reinterpret_cast<const float4*>(st0 + sl * 8)[0];
+      o.m = f.x;
+      o.Z = f.y;
+      o.T = f.z;
+      o.bx = f.w;
+      o.bi = reinterpret_cast<const int4*>(st0 + sl * 8)[1].x;
+      return o;
+    };
     RowState t;
     state_init(t);
-    for (int sl = 0; sl < a.slices; ++sl) {
-      const float4 v = reinterpret_cast<const float4*>(st0 + sl * 8)[0];
+    for (int sl = lane; sl < a.slices; sl += 32) state_merge(t, load_state(sl));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
       RowState o;
-      o.m = v.x;
-      o.Z = v.y;
-      o.T = v.z;
-      o.bx = v.w;
-      o.bi = reinterpret_cast<const int4*>(st0 + sl * 8)[1].x;
-      state_merge(t, o);
+      o.m = __shfl_xor_sync(0xffffffffu, t.m, off);
+      o.Z = __shfl_xor_sync(0xffffffffu, t.Z, off);
+      o.T = __shfl_xor_sync(0xffffffffu, t.T, off);
+      o.bx = __shfl_xor_sync(0xffffffffu, t.bx, off);
+      o.bi = __shfl_xor_sync(0xffffffffu, t.bi, off);
+      RowState lo = (lane & off) ? o : t;
+      const RowState hi = (lane & off) ? t : o;
+      state_merge(lo, hi);
+      t = lo;
     }
-    row_decision(a, row, t);
-    row_t = t;
+    if (lane == 0 && blockIdx.y == 0) row_decision(a, row, t);
+    for (int sl = lane; sl < a.slices; sl += 32) {
+      const float ms = st0[sl * 8], zs = st0[sl * 8 + 1];
+      wgt[sl] = (zs > 0.f && t.Z > 0.f) ? ex2_approx(ms - t.m) / t.Z : 0.f;
+    }
   }
   __syncthreads();
-  const RowState t = row_t;
-  for (int sl = threadIdx.x; sl < a.slices; sl += blockDim.x) {
-    const float ms = st0[sl * 8], zs = st0[sl * 8 + 1];
-    wgt[sl] = (zs > 0.f && t.Z > 0.f) ? ex2_approx(ms - t.m) / t.Z : 0.f;
-  }
-  __syncthreads();
-  const long long plane = (long long)a.rows * D / 4;  // float4s per split slab
-  const float4* p4 = reinterpret_cast<const float4*>(partials) + (long long)row * D / 4;
-  float4* o4 = reinterpret_cast<float4*>(soft) + (long long)row * D / 4;
-  for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sl = 0; sl < a.slices; ++sl) {
-      const float4 v = __ldcs(p4 + sl * plane + c);
-      const float w = wgt[sl];
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  if (!col) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kSoftRegSplits; ++j) {
+    if (j < a.slices) {
+      const float w = wgt[j];
+      acc.x = fmaf(w, v[j].x, acc.x);
+      acc.y = fmaf(w, v[j].y, acc.y);
+      acc.z = fmaf(w, v[j].z, acc.z);
+      acc.w = fmaf(w, v[j].w, acc.w);
     }
-    o4[c] = acc;
   }
+  for (int s0 = kSoftRegSplits; s0 < a.slices; s0 += 8) {
+    float4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j < a.slices) u[j] = __ldcs(p4 + (s0 + j) * plane);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < a.slices) {
+        const float w = wgt[s0 + j];
+        acc.x = fmaf(w, u[j].x, acc.x);
+        acc.y = fmaf(w, u[j].y, acc.y);
+        acc.z = fmaf(w, u[j].z, acc.z);
+        acc.w = fmaf(w, u[j].w, acc.w);
+      }
+    }
+  }
+  reinterpret_cast<float4*>(soft)[(long long)row * D / 4 + c] = acc;
 }
 
 template <typename T, int kThreads>
@@ -835,7 +874,8 @@ cudaError_t launch_sampler_slices(const SampleArgs& a, const void* logits, cudaS
 }
 
 cudaError_t launch_soft_reduce(const SampleArgs& a, const float* partials, float* soft, int D, cudaStream_t stream) {
-  soft_reduce_kernel<<<a.rows, 256, 0, stream>>>(a, partials, soft, D);
+  const int col_blocks = (D / 4 + kSoftReduceThreads - 1) / kSoftReduceThreads;
+  soft_reduce_kernel<<<dim3(a.rows, col_blocks, 1), kSoftReduceThreads, 0, stream>>>(a, partials, soft, D);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !(a.commit_mode & 1)) return e;
