@@ -810,10 +810,19 @@ static canvas_status attention_impl(const void* x, int dtype, int B, int C, int 
         maps.vpre_c = maps.vx_c;
       }
     } else {
+      // the one-SM kernel reads a value sub-block's d columns in one copy
       maps.kx_c = maps.kx;  // not read by the other kernels
-      maps.vx_c = maps.vx;
       maps.kpre_c = maps.kpre;
-      maps.vpre_c = maps.vpre;
+      st = make_map_bf16_chunked(&maps.vx_c, Vx, BH * pl.Tpad, d, 64, uint32_t(d / 64));
+      if (st != CANVAS_OK) return st;
+      if (max_prefix > 0) {
+        const uint64_t pool_rows = uint64_t(kv->num_pages) * Hkv * kv->page_tokens;
+        st = make_map_bf16_chunked(&maps.vpre_c, global ? kv->k_pool : kv->v_pool, pool_rows, d, 64,
+                                   uint32_t(d / 64));
+        if (st != CANVAS_OK) return st;
+      } else {
+        maps.vpre_c = maps.vx_c;
+      }
     }
     AttnTcArgs t;
     t.B = B;

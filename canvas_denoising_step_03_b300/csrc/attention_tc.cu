@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbarrier_init();
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.kpre);
-    tma_prefetch_desc(&maps.vpre);
+    tma_prefetch_desc(&maps.vpre_c);
     tma_prefetch_desc(&maps.kx);
-    tma_prefetch_desc(&maps.vx);
+    tma_prefetch_desc(&maps.vx_c);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -234,12 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         map = &maps.kx;
         return grp * a.Tpad + 64 * (s - sq.n_pre);
       };
+      // values through the 3D views (all DV columns of a 64-key sub-block in
+      // one copy) when they cover the whole head dimension
+      constexpr bool kV3 = K::DV == D;
       auto v_row = [&](int s, const CUtensorMap*& map) -> int {
         if (s < sq.n_pre) {
-          map = &maps.vpre;
+          map = kV3 ? &maps.vpre_c : &maps.vpre;
           return paged_row(a, b, hk, sq.s0 + 64 * s);
         }
-        map = &maps.vx;
+        map = kV3 ? &maps.vx_c : &maps.vx;
         return grp * a.Tpad + 64 * (s - sq.n_pre);
       };
       auto load_k = [&](int n) {
@@ -262,8 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!dst) break;
           const CUtensorMap* map;
           const int row = v_row(2 * kb + u, map);
-          for (int c = 0; c < K::DV / 64; ++c)
-            tma_load_2d(dst + c * 8192, map, &full[(it - 1) % K::NST], dvp * K::DV + c * 64, row);
+          if (kV3)
+            tma_load_3d(dst, map, &full[(it - 1) % K::NST], 0, row, 0);
+          else
+            for (int c = 0; c < K::DV / 64; ++c)
+              tma_load_2d(dst + c * 8192, map, &full[(it - 1) % K::NST], dvp * K::DV + c * 64, row);
         }
       };
       for (int n = 0; n < nb && alive; ++n) {

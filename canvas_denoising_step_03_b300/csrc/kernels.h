@@ -212,9 +212,10 @@ struct AttnTcArgs {
 };
 struct AttnTcMaps {
   CUtensorMap q, kpre, vpre, kx, vx;
-  // the 4-SM kernel: 3D views [64-column chunk][row][64] of the same tensors,
-  // so one copy brings a key box of 32 rows x all eight chunks, or a value
-  // box of 64 rows x two chunks
+  // 3D views [64-column chunk][row][64] of the same tensors, so one copy
+  // brings a key box of 32 rows x all eight chunks (4-SM kernel), or a value
+  // box of 64 rows x two chunks (4-SM kernel) / x all d / 64 chunks (one-SM
+  // kernel)
   CUtensorMap kpre_c, kx_c, vpre_c, vx_c;
 };
 size_t attention_tc_smem_bytes(int d);
