@@ -689,8 +689,12 @@ static canvas_status attention_impl(const void* x, int dtype, int B, int C, int 
   mark_start(CANVAS_KERNEL_PREP, stream);
   // 3. prefix keys of global layers, the prefix rows of the tail, zero padding:
   // independent of the projections and of the canvas rows (it writes other
-  // rows of the tail buffers), so it runs on a side stream beside steps 1-2
-  SideStream* side = side_stream();
+  // rows of the tail buffers), so a large one (global layers with long
+  // prefixes: 78 -> 62 us of preparation at prefix 32768) runs on a side
+  // stream beside steps 1-2; a small one stays on the call's stream and
+  // spares the fork and join
+  const bool big_prep = global && (long long)B * Hkv * max_prefix * d * 2 >= (32ll << 20);
+  SideStream* side = big_prep ? side_stream() : nullptr;
   cudaStream_t kstream = stream;
   if (side) {
     CANVAS_CUDA(cudaEventRecord(side->fork, stream));
