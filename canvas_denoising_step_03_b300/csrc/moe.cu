@@ -169,32 +169,46 @@ __global__ void __launch_bounds__(256) moe_act_kernel(const float4* __restrict__
   }
 }
 
-// One warp per token: out = sum_j w[t, j] * yg[slot[t, j]] (j in choice
-// order) + shared[t]  (fp32).
-__global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a) {
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp_global >= a.R) return;
-  const int t = warp_global;
-  for (int c = lane * 4; c < a.D; c += 128) {
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < a.k; ++j) {
-      const float w = a.topk_w[(size_t)t * a.k + j];
-      const float4 y = *reinterpret_cast<const float4*>(a.yg + (size_t)a.slot[(size_t)t * a.k + j] * a.D + c);
-      o.x = fmaf(w, y.x, o.x);
-      o.y = fmaf(w, y.y, o.y);
-      o.z = fmaf(w, y.z, o.z);
-      o.w = fmaf(w, y.w, o.w);
-    }
-    if (a.ys) {
-      const float4 s = *reinterpret_cast<const float4*>(a.ys + (size_t)t * a.D + c);
-      o.x += s.x;
-      o.y += s.y;
-      o.z += s.z;
-      o.w += s.w;
-    }
-    *reinterpret_cast<float4*>(a.out + (size_t)t * a.D + c) = o;
+// out = sum_j w[t, j] * yg[slot[t, j]] (j in choice order) + shared[t]
+// (fp32).  One block per (token, 512 columns): the token's weights and slots
+// are read once into shared memory, and each thread issues the loads of all
+// the token's choices for its four columns before it adds them.
+constexpr int kCombineCols = 512;
+constexpr int kMaxChoices = 16;
+__global__ void __launch_bounds__(kCombineCols / 4) moe_combine_kernel(MoeArgs a) {
+  __shared__ float w_s[kMaxChoices];
+  __shared__ int slot_s[kMaxChoices];
+  const int t = blockIdx.y;
+  if (threadIdx.x < a.k) {
+    w_s[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
+    slot_s[threadIdx.x] = a.slot[(size_t)t * a.k + threadIdx.x];
   }
+  __syncthreads();
+  const int c = blockIdx.x * kCombineCols + threadIdx.x * 4;
+  if (c >= a.D) return;
+  float4 y[kMaxChoices];
+#pragma unroll
+  for (int j = 0; j < kMaxChoices; ++j)
+    if (j < a.k) y[j] = __ldcs(reinterpret_cast<const float4*>(a.yg + (size_t)slot_s[j] * a.D + c));
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kMaxChoices; ++j) {
+    if (j < a.k) {
+      const float w = w_s[j];
+      o.x = fmaf(w, y[j].x, o.x);
+      o.y = fmaf(w, y[j].y, o.y);
+      o.z = fmaf(w, y[j].z, o.z);
+      o.w = fmaf(w, y[j].w, o.w);
+    }
+  }
+  if (a.ys) {
+    const float4 sh = *reinterpret_cast<const float4*>(a.ys + (size_t)t * a.D + c);
+    o.x += sh.x;
+    o.y += sh.y;
+    o.z += sh.z;
+    o.w += sh.w;
+  }
+  *reinterpret_cast<float4*>(a.out + (size_t)t * a.D + c) = o;
 }
 
 }  // namespace
@@ -220,7 +234,9 @@ cudaError_t launch_moe_act(const float* gate, const float* up, void* act, long l
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, cudaStream_t stream) {
-  moe_combine_kernel<<<(a.R * 32 + 255) / 256, 256, 0, stream>>>(a);
+  if (a.k > kMaxChoices || a.D % 4 != 0) return cudaErrorInvalidValue;
+  const dim3 grid((a.D + kCombineCols - 1) / kCombineCols, a.R, 1);
+  moe_combine_kernel<<<grid, kCombineCols / 4, 0, stream>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }
