@@ -10,6 +10,8 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -62,11 +64,24 @@ struct EventPair {
 };
 thread_local EventPair t_events[CANVAS_KERNEL_COUNT];
 
+// NVTX: a range around every compute call of the C ABI and one per timed
+// phase inside it (host-side markers; free when no tool is attached)
+const char* const kPhaseName[CANVAS_KERNEL_COUNT] = {"attention_core", "attention_prep", "sampler", "soft_emb_gemm"};
+static_assert(CANVAS_KERNEL_ATTENTION == 0 && CANVAS_KERNEL_PREP == 1 && CANVAS_KERNEL_SAMPLER == 2 &&
+                  CANVAS_KERNEL_SOFT_EMB == 3,
+              "phase names follow the timing ids");
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 inline void mark_start(int id, cudaStream_t s) {
+  nvtxRangePushA(kPhaseName[id]);
   if (t_events[id].start) cudaEventRecord(t_events[id].start, s);
 }
 inline void mark_stop(int id, cudaStream_t s) {
   if (t_events[id].stop) cudaEventRecord(t_events[id].stop, s);
+  nvtxRangePop();
 }
 
 canvas_status fail(canvas_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -492,6 +507,7 @@ canvas_status canvas_device_status(canvas_stream_t stream) {
 }
 
 canvas_status canvas_gelu_bf16(const float* in, void* out, size_t n, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_gelu_bf16");
   if (!in || !out) return fail(CANVAS_ERR_ARG, "canvas_gelu_bf16: null pointer");
   if (n % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_gelu_bf16: n must be a multiple of 8");
   if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
@@ -503,6 +519,7 @@ canvas_status canvas_gelu_bf16(const float* in, void* out, size_t n, canvas_stre
 
 canvas_status canvas_count_committed(const uint8_t* commit_mask, int rows, int canvas_len, int32_t* counts,
                                      canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_count_committed");
   if (!commit_mask || !counts) return fail(CANVAS_ERR_ARG, "canvas_count_committed: null pointer");
   if (rows < 1 || canvas_len < 1 || rows % canvas_len != 0)
     return fail(CANVAS_ERR_ARG, "canvas_count_committed: rows must be a multiple of canvas_len");
@@ -531,6 +548,7 @@ size_t canvas_gemm_workspace_size(int M, int N, int K) {
 
 canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float* C, int M, int N, int K,
                                int accumulate, void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_gemm_bf16");
   if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: null pointer");
   if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: bad shape");
   if (b_layout != 0 && b_layout != 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16: b_layout must be 0 or 1");
@@ -544,6 +562,7 @@ canvas_status canvas_gemm_bf16(const void* A, const void* B, int b_layout, float
 
 canvas_status canvas_gemm_bf16_to_bf16(const void* A, const void* B, int b_layout, void* C, int M, int N, int K,
                                        void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_gemm_bf16_to_bf16");
   if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: null pointer");
   if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: bad shape");
   if (b_layout != 0 && b_layout != 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_to_bf16: b_layout must be 0 or 1");
@@ -560,6 +579,7 @@ canvas_status canvas_gemm_bf16_to_bf16(const void* A, const void* B, int b_layou
 // ------------------------------------------------------------------ loop glue
 canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const float* soft_emb, int rows, int D,
                                  int V, void* x, float* x32, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_embed_input");
   if (!tokens || !E || !x) return fail(CANVAS_ERR_ARG, "canvas_embed_input: null pointer");
   if (rows < 1 || D < 1 || V < 1) return fail(CANVAS_ERR_ARG, "canvas_embed_input: bad shape");
   if (D % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_embed_input: D must be a multiple of 8");
@@ -572,6 +592,7 @@ canvas_status canvas_embed_input(const int32_t* tokens, const void* E, const flo
 }
 
 canvas_status canvas_cast_bf16(const float* in, void* out, size_t n, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_cast_bf16");
   if (!in || !out) return fail(CANVAS_ERR_ARG, "canvas_cast_bf16: null pointer");
   if (n % 8 != 0) return fail(CANVAS_ERR_UNSUPPORTED, "canvas_cast_bf16: n must be a multiple of 8");
   if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
@@ -589,6 +610,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[CANVAS_GEMM_NOA
 
 canvas_status canvas_gemm_bf16_noalloc(const void* A, const void* B, int b_layout, float* C, int M, int N, int K,
                                        int accumulate, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_gemm_bf16_noalloc");
   if (!A || !B || !C) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: null pointer");
   if (M < 1 || N < 1 || K < 1) return fail(CANVAS_ERR_ARG, "canvas_gemm_bf16_noalloc: bad shape");
   if (b_layout != 0 && b_layout != 1)
@@ -905,6 +927,7 @@ canvas_status canvas_attention(const void* x, int dtype, int B, int C, int D, co
                                float eps, const float* freq, int layer_type, const canvas_kv_cache* kv,
                                const int32_t* prefix_len, int max_prefix, int window, float scale, int v_unit_rms,
                                void* out, float* lse, void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_attention");
   return attention_impl(x, dtype, B, C, D, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, layer_type, kv,
                         prefix_len, max_prefix, window, scale, v_unit_rms, out, lse, workspace, ws_bytes, stream, 0);
 }
@@ -915,6 +938,7 @@ canvas_status canvas_attention_encode(const void* x, int dtype, int B, int C, in
                                       int layer_type, const canvas_kv_cache* kv, const int32_t* prefix_len,
                                       int max_prefix, int window, float scale, int v_unit_rms, void* out, float* lse,
                                       void* workspace, size_t ws_bytes, canvas_stream_t stream) {
+  NvtxRange nvtx_range("canvas_attention_encode");
   return attention_impl(x, dtype, B, C, D, W_q, W_k, W_v, Hq, Hkv, d, gamma_q, gamma_k, eps, freq, layer_type, kv,
                         prefix_len, max_prefix, window, scale, v_unit_rms, out, lse, workspace, ws_bytes, stream, 1);
 }
@@ -943,6 +967,7 @@ canvas_status canvas_kv_append(const void* x, int dtype, int B, int C, int D, co
                                int Hkv, int d, const float* gamma_k, float eps, const float* freq, int layer_type,
                                const canvas_kv_cache* kv, int32_t* prefix_len, int max_prefix, void* workspace,
                                size_t ws_bytes, canvas_stream_t stream_) {
+  NvtxRange nvtx_range("canvas_kv_append");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const size_t need = canvas_kv_append_workspace_size(dtype, B, C, D, Hkv, d, layer_type);
   if (need == 0) return fail(CANVAS_ERR_ARG, "canvas_kv_append: invalid shape, dtype or layer type");
@@ -1060,6 +1085,7 @@ canvas_status canvas_moe(const void* x, int R, int D, const void* router, int E,
                          const void* W_gate, const void* W_up, const void* W_down, int F, const void* Ws_gate,
                          const void* Ws_up, const void* Ws_down, int Fs, float* out, int32_t* topk_idx,
                          float* topk_w, void* workspace, size_t ws_bytes, canvas_stream_t stream_) {
+  NvtxRange nvtx_range("canvas_moe");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!moe_shape_ok(R, D, E, F, k, Fs))
     return fail(CANVAS_ERR_ARG, "canvas_moe: shape (D, F, Fs multiples of 8; E a multiple of 8 up to 256; 1 <= k <= 16, k <= E)");
@@ -1150,6 +1176,7 @@ canvas_status canvas_sample(const void* logits, int dtype, int rows, int V, cons
                             uint8_t* commit_mask, float* entropy, float* confidence, int32_t* argmax,
                             void* probs_out, int probs_dtype, float* soft_emb, void* workspace, size_t ws_bytes,
                             canvas_stream_t stream_) {
+  NvtxRange nvtx_range("canvas_sample");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (dtype != CANVAS_BF16 && dtype != CANVAS_FP32) return fail(CANVAS_ERR_ARG, "canvas_sample: dtype");
   if (rows < 1 || V < 1 || D < 1) return fail(CANVAS_ERR_ARG, "canvas_sample: bad shape");
