@@ -140,6 +140,28 @@ def test_temperature_prefix_mode_and_frozen(cv):
         compare(cv, s, run, ref)
 
 
+@pytest.mark.parametrize("V", [4096, 262136])
+def test_deferred_and_cluster_paths_agree(cv, V):
+    """Without probs_out a bf16 call normalises each vocabulary range after the
+    soft-embedding product; with probs_out the cluster kernel writes the
+    probabilities first.  Both come from the same per-row state: entropy and
+    confidence to fp32 merge-order rounding, argmax, mask and tokens exactly,
+    the soft embeddings to the bf16 rounding of the probabilities."""
+    s = _peaked_small("bf16", rows=48, V=V, seed=21)
+    deferred = SampleRun(cv, s)
+    cluster = SampleRun(cv, s, probs_dtype="bf16")
+    np.testing.assert_array_equal(deferred.amax.cpu().numpy(), cluster.amax.cpu().numpy())
+    np.testing.assert_array_equal(deferred.mask.cpu().numpy(), cluster.mask.cpu().numpy())
+    np.testing.assert_array_equal(deferred.tokens.cpu().numpy(), cluster.tokens.cpu().numpy())
+    np.testing.assert_allclose(deferred.ent.cpu().numpy(), cluster.ent.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(deferred.conf.cpu().numpy(), cluster.conf.cpu().numpy(), rtol=1e-5, atol=1e-9)
+    a = deferred.soft.cpu().numpy().astype(np.float64)
+    b = cluster.soft.cpu().numpy().astype(np.float64)
+    assert np.isfinite(a).all()
+    rf = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rf <= 2e-3, rf
+
+
 def test_renoise_tokens_independent_of_launch_shape(cv):
     # the same rows sampled as part of a larger batch get the same renoise draws
     s = _peaked_small("bf16", rows=32, V=1024, seed=4)
