@@ -126,7 +126,7 @@ def attn_bar(want):
     return np.maximum(BF16_MAX, 0.5 * bf16_spacing(want))
 
 
-def judge_attention(name, got, want, slack, want64=None, record=True):
+def attention_bar(name, got, want, slack, want64=None, record=True):
     """Hold a bf16 attention output to the bar above; returns the record.
 
     got: device output (fp64 of the stored bf16); want: oracle, bf16 storage

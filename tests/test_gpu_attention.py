@@ -2,7 +2,7 @@
 
 Tolerances: bf16 calls -- max |err| <= 2e-2 and relative Frobenius error
 <= 5e-3 (the bar set for the attention output in bf16), with the two
-refinements of canvas_harness.judge_attention (half a bf16 spacing for
+refinements of canvas_harness.attention_bar (half a bf16 spacing for
 |value| >= 8; the oracle's rounding slack downstream of rounding ties, on at
 most MAX_FRAC_OVER of the elements); each case records plain max |err|, the
 number of elements above 2e-2, the number that needed slack, and the distance
@@ -22,7 +22,7 @@ import pytest
 import torch
 
 import canvas_workloads as wl
-from canvas_harness import SLACK_EPS, AttnCase, attn_errors, judge_attention, oracle_attention
+from canvas_harness import SLACK_EPS, AttnCase, attn_errors, attention_bar, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,7 @@ def check(cv, cfg, rows=None, v_unit_rms=False, page_seed=1234, name=None):
     if cfg.dtype == "bf16":
         want, want_lse, slack = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms, slack_eps=SLACK_EPS)
         want64, _ = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms, storage="fp64")
-        rec = judge_attention(name or cfg.name, got, want, slack, want64)
+        rec = attention_bar(name or cfg.name, got, want, slack, want64)
         mx, rf = rec["max_abs_err"], rec["rel_fro"]
     else:
         want, want_lse = oracle_attention(inp, rows=rows, v_unit_rms=v_unit_rms)

@@ -6,7 +6,7 @@ paged cache (canvas_kv_append: sliding layers append final keys and values,
 global layers the raw shared rows), and the next canvas is attended in
 decode mode over the extended prefix.
 
-Bars: the attention bar of canvas_harness.judge_attention for both attention
+Bars: the attention bar of canvas_harness.attention_bar for both attention
 calls; the appended cache rows bit-exact against the oracle's stored rows
 except at rounding ties (where the row's pre-rounding value lies within the
 path's fp32 error of a bf16 midpoint: either neighbour is a correct stored
@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import canvas_workloads as wl
-from canvas_harness import SLACK_EPS, judge_attention, to_device
+from canvas_harness import SLACK_EPS, attention_bar, to_device
 from oracle import attention as oatt
 
 pytestmark = pytest.mark.gpu
@@ -89,7 +89,7 @@ def test_encode_commit_then_decode_the_next_canvas(cv, spec):
                                            causal=True)
     want64, _ = oatt.canvas_attention(*args, ck0, cv0, P0, cfg.window, storage="fp64", causal=True)
     got = out.float().cpu().numpy().astype(np.float64)
-    judge_attention(f"{cfg.name} block, encode mode", got, want, slack, want64)
+    attention_bar(f"{cfg.name} block, encode mode", got, want, slack, want64)
     # the two modes differ on this workload by far more than the bar: the
     # comparison above tells them apart
     dec, _ = oatt.canvas_attention(*args, ck0, cv0, P0, cfg.window, storage="bf16")
@@ -152,7 +152,7 @@ def test_encode_commit_then_decode_the_next_canvas(cv, spec):
              cfg.layer, ck, cvv, P0 + C, cfg.window)
     want2, _, slack2 = oatt.canvas_attention(*args2, storage="bf16", slack_eps=SLACK_EPS, cache_dk=dck, cache_dv=dcv)
     want2_64, _ = oatt.canvas_attention(*args2, storage="fp64")
-    judge_attention(f"{cfg.name} next canvas over the committed block", out2.float().cpu().numpy().astype(np.float64),
+    attention_bar(f"{cfg.name} next canvas over the committed block", out2.float().cpu().numpy().astype(np.float64),
                     want2, slack2, want2_64)
 
 

@@ -9,7 +9,7 @@ every stage of every step runs on the device from the oracle's own input to
 that stage (oracle values feed the device, never the reverse) and its output
 is held to the bar of that stage --
   attention layer  the bar of test_gpu_attention.py
-                   (canvas_harness.judge_attention) against the oracle's
+                   (canvas_harness.attention_bar) against the oracle's
                    output before its bf16 store: |err| <= max(2e-2, half a
                    bf16 spacing of the value) + rounding slack on at most
                    MAX_FRAC_OVER of the elements, rel-Fro <= 5e-3 (the
@@ -28,7 +28,7 @@ import pytest
 import torch
 
 import canvas_workloads as wl
-from canvas_harness import SLACK_EPS, judge_attention
+from canvas_harness import SLACK_EPS, attention_bar
 from oracle import attention as oatt
 from oracle import loop as oloop
 from oracle import sampler as osamp
@@ -108,7 +108,7 @@ def check_step(cv, run, ref, cfg, step, frozen, ftok, rows, run_wo, E_exact, lay
         want64 = None
         if layers is not None:
             want64 = _fp64_layer(layers, k, xin.reshape(B, C, D), B, C)
-        rec = judge_attention(f"{cfg.name} step {step} layer {k} ({layers[k]['layer'] if layers else ''})", got,
+        rec = attention_bar(f"{cfg.name} step {step} layer {k} ({layers[k]['layer'] if layers else ''})", got,
                               want, slack, want64)
         # residual add on the oracle's fp32 stream and its stored attention
         # output: fp32 accumulation over K terms is within gamma_K * sum |terms|
@@ -227,7 +227,7 @@ def test_loop_workload_long_prefix_layers(cv, prefix):
                 L["freq"], L["layer"], L["cache_k"], L["cache_v"], np.full(B, L["prefix"]), L["window"])
         want, _, slack = oatt.canvas_attention(*args, storage="bf16", rows=sub, slack_eps=SLACK_EPS)
         want64, _ = oatt.canvas_attention(*args, storage="fp64", rows=sub)
-        judge_attention(f"{cfg.name} step 0 layer {k} ({L['layer']}, {n} sampled canvas rows)", got, want, slack,
+        attention_bar(f"{cfg.name} step 0 layer {k} ({L['layer']}, {n} sampled canvas rows)", got, want, slack,
                         want64)
 
 

@@ -2,7 +2,7 @@
 
 Routing: the chosen experts bit-exact, in order, except for tokens whose k-th
 and (k+1)-th router scores lie within the fp32 error of the scores (a tie:
-logged and excluded, the rule the benchmark spec applies to tokens); weights
+logged and excluded, as for sampled tokens at an entropy tie); weights
 within 1e-5 relative.  Output: every element within a bound computed from
 the arithmetic -- the fp32 recursive-summation bound of each product
 (gamma_K sum |terms|), the bf16 activation's rounding ties (an activation
