@@ -501,6 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
       tc_fence_after();
     }
+    // the combine may be scheduled now (it waits for this grid to finish)
+    if (warp == 2 && lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // ---------------- epilogue: the pair's partial sums, then each warp
     // writes its half of the row's value columns
     float l_row = l;
@@ -997,6 +999,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
       alive = mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, flags);
       tc_fence_after();
     }
+    // the combine may be scheduled now (it waits for this grid to finish)
+    if (warp == 2 && lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the two key halves' sums, through the exchange slot of block nb
     float l_row = l;
     if (alive) {
@@ -1067,6 +1071,9 @@ __global__ void __launch_bounds__(kThreads4, 1)
 // every split before it adds them (in split order).
 constexpr int kMaxCombineSplits = 32;
 __global__ void __launch_bounds__(256) attention_combine_kernel(AttnTcArgs a) {
+  // launched as a programmatic dependent of the attention kernel: wait for
+  // all of its blocks and their stores before reading the partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int GC = a.G * a.C;
   const int lane = threadIdx.x & 31;
   const long long wrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -1192,9 +1199,19 @@ cudaError_t launch_attention_tc(const AttnTcMaps& maps, const AttnTcArgs& a, cud
 
 cudaError_t launch_attention_combine(const AttnTcArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.B * a.Hkv * a.G * a.C;
-  attention_combine_kernel<<<int((rows + 7) / 8), 256, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((rows + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, attention_combine_kernel, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace canvas
